@@ -1,0 +1,15 @@
+"""Shared pytest configuration.
+
+Tests marked ``gpu`` need a GB300 and the built CUDA library; everything else
+runs on a CPU-only machine (``pytest -m "not gpu"``).
+"""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103) and the built library")
