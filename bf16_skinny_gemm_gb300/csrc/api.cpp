@@ -1,0 +1,382 @@
+// Host side of the BF16 skinny GEMM library: argument checks, plan selection,
+// launch.  The C ABI is declared (and documented) in include/sgemm_skinny.h.
+//
+// Dispatch follows the plan tables of vLLM PR #62949 (Details: per-shape
+// configs from a sweep, keyed by the local (N, K) and M) and vLLM PR #65306
+// (Details: table keyed by capability and local (N, K)).  Here the table is
+// compiled in for sm_103 only, and shapes without an entry get a heuristic
+// plan instead of another library's GEMM.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+#include "internal.h"
+
+namespace {
+
+using sk::KernelInfo;
+
+struct TableEntry {
+    int N, K, M;
+    int variant, threads, R, LPR, U, split, stages, ctas_per_sm;
+};
+
+// Plans from the offline sweep (generated file; see the package's sweep module).
+const TableEntry kTable[] = {
+#include "plan_table.inc"
+    {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0}  // sentinel
+};
+const int kTableSize = static_cast<int>(sizeof(kTable) / sizeof(kTable[0])) - 1;
+
+constexpr int kThreadChoices[] = {256, 128};
+constexpr int kNumThreadChoices = 2;
+constexpr size_t kMaxSmem = 227 * 1024;
+constexpr size_t kDefaultWorkspace = 16u << 20;
+
+const KernelInfo *table_for_m(int M) {
+    switch (M) {
+        case 1: return sk::kKernelsM1;
+        case 2: return sk::kKernelsM2;
+        case 3: return sk::kKernelsM3;
+        case 4: return sk::kKernelsM4;
+        default: return nullptr;
+    }
+}
+
+const KernelInfo *find_kernel(int variant, int M, int R, int LPR, int U) {
+    const KernelInfo *t = table_for_m(M);
+    if (!t) return nullptr;
+    for (int i = 0; i < sk::kKernelCountPerM; ++i)
+        if (t[i].variant == variant && t[i].R == R && t[i].LPR == LPR && t[i].U == U) return &t[i];
+    return nullptr;
+}
+
+struct DeviceState {
+    bool probed = false;
+    bool supported = false;
+    int sms = 0;
+    float *ws = nullptr;
+    size_t ws_bytes = 0;
+    std::map<std::tuple<const void *, int, size_t>, int> occupancy;
+    std::map<const void *, bool> smem_attr_set;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_dev;
+
+// kps: K elements per split, a multiple of 8; every split non-empty.
+int split_kps(int K, int split) {
+    const int chunks = K / 8;
+    const int per = (chunks + split - 1) / split;
+    return per * 8;
+}
+
+sgemm_status_t check_plan(const sgemm_plan_t &p, int M, int N, int K) {
+    (void)N;
+    if (p.variant != SGEMM_VARIANT_LDG) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (p.threads < 32 || p.threads > sk::kMaxThreads || p.threads % 32) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (p.vec_bytes != 16 || p.stages != 0) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (p.split_k < 1 || p.split_k > 64) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (p.ctas_per_sm < 0 || p.ctas_per_sm > 32) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (!find_kernel(p.variant, M, p.rows_per_warp, p.lanes_per_row, p.k_unroll))
+        return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    const int kps = split_kps(K, p.split_k);
+    if (static_cast<long long>(p.split_k - 1) * kps >= K) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (static_cast<size_t>(M) * kps * 2 > kMaxSmem) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    return SGEMM_OK;
+}
+
+sgemm_plan_t make_plan(int variant, int threads, int R, int LPR, int U, int split, int stages,
+                       int ctas, int id) {
+    sgemm_plan_t p;
+    p.variant = variant;
+    p.threads = threads;
+    p.rows_per_warp = R;
+    p.lanes_per_row = LPR;
+    p.k_unroll = U;
+    p.vec_bytes = 16;
+    p.split_k = split;
+    p.stages = stages;
+    p.ctas_per_sm = ctas;
+    p.id = id;
+    return p;
+}
+
+sgemm_plan_t heuristic_plan(int N, int K, int M) {
+    (void)N;
+    int R, LPR, U;
+    if (K <= 128) {
+        R = 2, LPR = 16, U = 1;
+    } else if (K <= 256) {
+        R = 2, LPR = 32, U = 2;
+    } else if (M <= 2) {
+        R = 1, LPR = 32, U = 8;
+    } else {
+        R = 2, LPR = 32, U = 4;
+    }
+    int split = 1;
+    const size_t budget = 96 * 1024;  // x slice per CTA, leaves room for two CTAs per SM
+    if (M >= 1 && K >= 8) {
+        const size_t xbytes = static_cast<size_t>(M) * K * 2;
+        split = static_cast<int>((xbytes + budget - 1) / budget);
+        split = std::max(1, std::min(split, 64));
+    }
+    return make_plan(SGEMM_VARIANT_LDG, 256, R, LPR, U, split, 0, 0, -1);
+}
+
+sgemm_status_t probe_device(int *dev_out, DeviceState **st_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &st = g_dev[dev];
+    if (!st.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SGEMM_ERR_CUDA;
+        st.probed = true;
+        st.supported = (major == 10 && minor == 3);
+        st.sms = sms;
+    }
+    if (!st.supported) return SGEMM_ERR_UNSUPPORTED_DEVICE;
+    *dev_out = dev;
+    *st_out = &st;
+    return SGEMM_OK;
+}
+
+// Requires g_mu held.
+sgemm_status_t ensure_workspace(DeviceState &st, size_t bytes, cudaStream_t stream) {
+    if (st.ws && st.ws_bytes >= bytes) return SGEMM_OK;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return SGEMM_ERR_NO_WORKSPACE;
+    if (cap != cudaStreamCaptureStatusNone) return SGEMM_ERR_NO_WORKSPACE;
+    size_t want = std::max(bytes, kDefaultWorkspace);
+    if (st.ws) {
+        // older launches may still read the old scratch
+        if (cudaDeviceSynchronize() != cudaSuccess) return SGEMM_ERR_CUDA;
+        cudaFree(st.ws);
+        st.ws = nullptr;
+        st.ws_bytes = 0;
+    }
+    void *p = nullptr;
+    if (cudaMalloc(&p, want) != cudaSuccess) return SGEMM_ERR_CUDA;
+    st.ws = static_cast<float *>(p);
+    st.ws_bytes = want;
+    return SGEMM_OK;
+}
+
+// Requires g_mu held.
+int occupancy(DeviceState &st, const void *fn, int threads, size_t smem) {
+    auto key = std::make_tuple(fn, threads, smem);
+    auto it = st.occupancy.find(key);
+    if (it != st.occupancy.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess) n = 1;
+    n = std::max(n, 1);
+    st.occupancy[key] = n;
+    return n;
+}
+
+sgemm_status_t validate_common(int M, int N, int K, int batch) {
+    if (M < 1 || M > sk::kMaxM || N < 1 || K < 1) return SGEMM_ERR_INVALID_ARG;
+    if (batch < 1 || batch > sk::kMaxBatch) return SGEMM_ERR_INVALID_ARG;
+    if (K % 8) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    return SGEMM_OK;
+}
+
+sgemm_status_t validate_item(const sgemm_pair_t &it, int N, int K) {
+    if (!it.x || !it.W || !it.y) return SGEMM_ERR_INVALID_ARG;
+    if (it.ldx < K || it.ldy < N) return SGEMM_ERR_INVALID_ARG;
+    const uintptr_t ax = reinterpret_cast<uintptr_t>(it.x);
+    const uintptr_t aw = reinterpret_cast<uintptr_t>(it.W);
+    const uintptr_t ay = reinterpret_cast<uintptr_t>(it.y);
+    if ((ax | aw) & 15u) return SGEMM_ERR_MISALIGNED;  // 128-bit loads
+    if (ay & 1u) return SGEMM_ERR_MISALIGNED;          // 16-bit stores
+    if (it.ldx % 8) return SGEMM_ERR_MISALIGNED;
+    return SGEMM_OK;
+}
+
+sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
+                   const sgemm_plan_t *plan_in, cudaStream_t stream) {
+    sgemm_status_t s = validate_common(M, N, K, batch);
+    if (s != SGEMM_OK) return s;
+    if (!items) return SGEMM_ERR_INVALID_ARG;
+    for (int b = 0; b < batch; ++b) {
+        s = validate_item(items[b], N, K);
+        if (s != SGEMM_OK) return s;
+    }
+    const sgemm_plan_t plan = plan_in ? *plan_in : sgemm_plan_select(N, K, M);
+    s = check_plan(plan, M, N, K);
+    if (s != SGEMM_OK) return s;
+
+    int dev = 0;
+    DeviceState *st = nullptr;
+    s = probe_device(&dev, &st);
+    if (s != SGEMM_OK) return s;
+
+    const KernelInfo *ki = find_kernel(plan.variant, M, plan.rows_per_warp, plan.lanes_per_row,
+                                       plan.k_unroll);
+    const int split = plan.split_k;
+    const int kps = split_kps(K, split);
+    const size_t smem = static_cast<size_t>(M) * kps * 2;
+
+    sk::Params prm;
+    std::memset(&prm, 0, sizeof(prm));
+    for (int b = 0; b < batch; ++b) {
+        prm.item[b].x = items[b].x;
+        prm.item[b].W = items[b].W;
+        prm.item[b].y = items[b].y;
+        prm.item[b].ldx = items[b].ldx;
+        prm.item[b].ldy = items[b].ldy;
+    }
+    prm.N = N;
+    prm.K = K;
+    prm.kps = kps;
+    prm.split = split;
+    const int rows_per_task = (32 / plan.lanes_per_row) * plan.rows_per_warp;
+    prm.row_groups = (N + rows_per_task - 1) / rows_per_task;
+
+    int grid_x = 0;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (split > 1) {
+            const size_t need = static_cast<size_t>(batch) * split * M * N * sizeof(float);
+            s = ensure_workspace(*st, need, stream);
+            if (s != SGEMM_OK) return s;
+            prm.ws = st->ws;
+        }
+        if (!st->smem_attr_set[ki->fn]) {
+            if (cudaFuncSetAttribute(ki->fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kMaxSmem)) != cudaSuccess)
+                return SGEMM_ERR_CUDA;
+            st->smem_attr_set[ki->fn] = true;
+        }
+        const int occ = plan.ctas_per_sm > 0 ? plan.ctas_per_sm
+                                             : occupancy(*st, ki->fn, plan.threads, smem);
+        const int warps = plan.threads / 32;
+        const long long need_ctas = (prm.row_groups + warps - 1) / warps;
+        const long long slots = std::max<long long>(1, static_cast<long long>(st->sms) * occ /
+                                                           (static_cast<long long>(split) * batch));
+        grid_x = static_cast<int>(std::max<long long>(1, std::min(need_ctas, slots)));
+    }
+
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_x), static_cast<unsigned>(split),
+                       static_cast<unsigned>(batch));
+    cfg.blockDim = dim3(static_cast<unsigned>(plan.threads), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    void *args[] = {&prm};
+    if (cudaLaunchKernelExC(&cfg, ki->fn, args) != cudaSuccess) return SGEMM_ERR_CUDA;
+
+    if (split > 1) {
+        const long long total = static_cast<long long>(batch) * M * N;
+        int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 8LL * st->sms));
+        cudaLaunchConfig_t rc;
+        std::memset(&rc, 0, sizeof(rc));
+        rc.gridDim = dim3(static_cast<unsigned>(std::max(blocks, 1)), 1, 1);
+        rc.blockDim = dim3(256, 1, 1);
+        rc.dynamicSmemBytes = 0;
+        rc.stream = stream;
+        int batch_arg = batch;
+        void *rargs[] = {&prm, &batch_arg};
+        if (cudaLaunchKernelExC(&rc, sk::kReduceKernels[M], rargs) != cudaSuccess)
+            return SGEMM_ERR_CUDA;
+    }
+    return SGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sgemm_plan_t sgemm_plan_select(int N, int K, int M) {
+    for (int i = 0; i < kTableSize; ++i) {
+        const TableEntry &e = kTable[i];
+        if (e.N == N && e.K == K && e.M == M) {
+            sgemm_plan_t p = make_plan(e.variant, e.threads, e.R, e.LPR, e.U, e.split, e.stages,
+                                       e.ctas_per_sm, i);
+            if (check_plan(p, M, N, K) == SGEMM_OK) return p;
+        }
+    }
+    return heuristic_plan(N, K, M);
+}
+
+int sgemm_plan_count(void) { return sk::kKernelCountPerM * kNumThreadChoices; }
+
+sgemm_status_t sgemm_plan_get(int index, sgemm_plan_t *plan) {
+    if (!plan || index < 0 || index >= sgemm_plan_count()) return SGEMM_ERR_INVALID_ARG;
+    const KernelInfo &k = sk::kKernelsM1[index / kNumThreadChoices];
+    *plan = make_plan(k.variant, kThreadChoices[index % kNumThreadChoices], k.R, k.LPR, k.U, 1, 0,
+                      0, -1);
+    return SGEMM_OK;
+}
+
+sgemm_status_t sgemm_plan_check(const sgemm_plan_t *plan, int M, int N, int K) {
+    if (!plan) return SGEMM_ERR_INVALID_ARG;
+    sgemm_status_t s = validate_common(M, N, K, 1);
+    if (s != SGEMM_OK) return s;
+    return check_plan(*plan, M, N, K);
+}
+
+sgemm_status_t sgemm_bf16_skinny_ex(const sgemm_bf16_t *x, long long ldx, const sgemm_bf16_t *W,
+                                    sgemm_bf16_t *y, long long ldy, int M, int N, int K,
+                                    const sgemm_plan_t *plan, sgemm_stream_t stream) {
+    sgemm_pair_t it;
+    it.x = x;
+    it.W = W;
+    it.y = y;
+    it.ldx = ldx;
+    it.ldy = ldy;
+    return run(&it, 1, M, N, K, plan, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sgemm_status_t sgemm_bf16_skinny(const sgemm_bf16_t *x, const sgemm_bf16_t *W, sgemm_bf16_t *y,
+                                 int M, int N, int K, sgemm_stream_t stream) {
+    return sgemm_bf16_skinny_ex(x, K, W, y, N, M, N, K, nullptr, stream);
+}
+
+sgemm_status_t sgemm_bf16_skinny_batched_ex(const sgemm_pair_t *items, int batch, int M, int N,
+                                            int K, const sgemm_plan_t *plan,
+                                            sgemm_stream_t stream) {
+    return run(items, batch, M, N, K, plan, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sgemm_status_t sgemm_bf16_skinny_batched(const sgemm_pair_t *items, int batch, int M, int N, int K,
+                                         sgemm_stream_t stream) {
+    return run(items, batch, M, N, K, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sgemm_status_t sgemm_init(void) {
+    int dev = 0;
+    DeviceState *st = nullptr;
+    sgemm_status_t s = probe_device(&dev, &st);
+    if (s != SGEMM_OK) return s;
+    std::lock_guard<std::mutex> lk(g_mu);
+    return ensure_workspace(*st, kDefaultWorkspace, nullptr);
+}
+
+const char *sgemm_status_string(sgemm_status_t status) {
+    switch (status) {
+        case SGEMM_OK: return "ok";
+        case SGEMM_ERR_INVALID_ARG: return "invalid argument";
+        case SGEMM_ERR_UNSUPPORTED_SHAPE: return "unsupported shape or plan";
+        case SGEMM_ERR_MISALIGNED: return "misaligned pointer or row stride";
+        case SGEMM_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+        case SGEMM_ERR_NO_WORKSPACE: return "split-K scratch missing during stream capture";
+        case SGEMM_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+const char *sgemm_version(void) { return "0.1.0"; }
+
+}  // extern "C"

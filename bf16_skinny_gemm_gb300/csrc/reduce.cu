@@ -1,0 +1,17 @@
+// Split-K second-pass kernels (one per M) and the per-M kernel count.
+#include "kernel_table.cuh"
+
+namespace sk {
+
+#define SK_COUNT_ONE(M, R, LPR, U) +1
+const int kKernelCountPerM = 0 SK_LDG_CONFIGS(SK_COUNT_ONE, 1);
+
+const void *const kReduceKernels[kMaxM + 1] = {
+    nullptr,
+    reinterpret_cast<const void *>(&splitk_reduce_kernel<1>),
+    reinterpret_cast<const void *>(&splitk_reduce_kernel<2>),
+    reinterpret_cast<const void *>(&splitk_reduce_kernel<3>),
+    reinterpret_cast<const void *>(&splitk_reduce_kernel<4>),
+};
+
+}  // namespace sk

@@ -1,0 +1,168 @@
+/*
+ * sgemm_skinny.h -- C ABI of the GB300 (sm_103a) BF16 skinny GEMM library.
+ *
+ *     y[M,N] = x[M,K] . W[N,K]^T        1 <= M <= 4, BF16 in, FP32 accumulate, BF16 out
+ *
+ * The operation is the F.linear projection of a decode step with M tokens, as
+ * used for the unquantized attention, shared-expert and LM-head projections in
+ * vLLM PR #62949 ("SM121 skinny-GEMM plans for the GLM-5.3-Flash BF16 decode
+ * projections", Overview and Validation table) and vLLM PR #65306 ("Add SM90
+ * skinny GEMM plans for the BF16 decode projections", Overview).  Each weight
+ * is read exactly once per call, so the call is bound by HBM bandwidth.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Element type: raw BF16 bit patterns (sgemm_bf16_t).  Products are formed
+ *   exactly and accumulated in FP32; each output is rounded once to BF16,
+ *   round-to-nearest-even.  The accumulation order depends only on (N, K) and
+ *   the plan, never on M or on the data, so a call is deterministic: the same
+ *   inputs and plan give bitwise-identical outputs, and row m of an M-row call
+ *   equals the 1-row call on x[m,:] under the same plan.
+ * - Layout: x is row-major [M,K] with row stride ldx elements (ldx >= K; the
+ *   plain call uses ldx = K); W is row-major [N,K], contiguous (the F.linear
+ *   weight layout); y is row-major [M,N] with row stride ldy (>= N).
+ * - Memory: every array pointer is a DEVICE pointer on the calling thread's
+ *   current CUDA device, owned by the caller.  The library keeps no pointer
+ *   after a call returns, so weights may be refreshed in place between calls
+ *   or between CUDA-graph replays (the in-place refresh rule of vLLM PR #57617,
+ *   "Batch paired KDA gate projections (f_b_proj/g_b_proj) into one bmm",
+ *   Purpose and source).
+ * - Alignment: x and W must be 16-byte aligned, K a multiple of 8 and ldx a
+ *   multiple of 8, so that every row of x and W starts on a 16-byte boundary
+ *   (they are read with 128-bit loads).  y is written element by element and
+ *   needs only 2-byte alignment; ldy may be any value >= N.
+ * - Streams: work is enqueued asynchronously on `stream` (NULL = the legacy
+ *   default stream); nothing blocks the host.  A call neither allocates nor
+ *   synchronizes unless it needs split-K scratch that does not exist yet (see
+ *   sgemm_init), so it can be captured into a CUDA graph.
+ * - Errors: arguments are checked on the host before anything is enqueued;
+ *   a bad argument returns a status and launches nothing.  There is no CPU
+ *   fallback and no fallback to another GEMM library.  A failed launch
+ *   returns SGEMM_ERR_CUDA (the CUDA error is left for cudaGetLastError).
+ * - Devices: only compute capability 10.3 (GB300, sm_103) is accepted.
+ */
+#ifndef SGEMM_SKINNY_H
+#define SGEMM_SKINNY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Raw BF16 bits: sign(1) | exponent(8) | fraction(7). */
+typedef uint16_t sgemm_bf16_t;
+
+/* Identical to cudaStream_t / CUstream; declared here so that this header
+ * needs no CUDA header. */
+typedef struct CUstream_st *sgemm_stream_t;
+
+typedef enum {
+    SGEMM_OK = 0,
+    SGEMM_ERR_INVALID_ARG = 1,        /* null pointer, M outside 1..4, N or K < 1, bad ld, batch */
+    SGEMM_ERR_UNSUPPORTED_SHAPE = 2,  /* K not a multiple of 8, or a plan that cannot run it */
+    SGEMM_ERR_MISALIGNED = 3,         /* x or W not 16-byte aligned, ldx % 8 != 0, y odd */
+    SGEMM_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
+    SGEMM_ERR_NO_WORKSPACE = 5,       /* split-K scratch missing while the stream is capturing */
+    SGEMM_ERR_CUDA = 6                /* a CUDA runtime call or launch failed */
+} sgemm_status_t;
+
+/* One launch configuration ("plan") of the kernel.  The fields are the tuning
+ * knobs of the skinny-GEMM plan tables in vLLM PR #62949 (Details: block_size,
+ * outputs_per_block, k_unroll, vector_width) extended with a split-K factor and
+ * a pipeline depth. */
+typedef struct {
+    int variant;          /* kernel family, see SGEMM_VARIANT_* */
+    int threads;          /* threads per CTA (a multiple of 32) */
+    int rows_per_warp;    /* output rows n a warp accumulates at once */
+    int lanes_per_row;    /* lanes sharing one row: 32, 16 or 8 (16/8 suit small K) */
+    int k_unroll;         /* 16-byte W loads per row per lane kept in flight */
+    int vec_bytes;        /* bytes per W load: 16 */
+    int split_k;          /* K split across this many CTAs (1 = none) */
+    int stages;           /* shared-memory pipeline depth (0 = register streaming) */
+    int ctas_per_sm;      /* resident CTAs per SM the grid is sized for (0 = occupancy max) */
+    int id;               /* index in the compiled plan table, or -1 for a heuristic plan */
+} sgemm_plan_t;
+
+enum {
+    SGEMM_VARIANT_LDG = 0  /* W streamed with 128-bit non-allocating loads into registers,
+                              x staged in shared memory, warp-shuffle reduction */
+};
+
+/* y = x . W^T for contiguous x [M,K] and y [M,N].  Plan: sgemm_plan_select(N, K, M). */
+sgemm_status_t sgemm_bf16_skinny(const sgemm_bf16_t *x, const sgemm_bf16_t *W, sgemm_bf16_t *y,
+                                 int M, int N, int K, sgemm_stream_t stream);
+
+/* As sgemm_bf16_skinny with row strides for x and y and an optional plan
+ * (NULL = sgemm_plan_select).  A plan that does not fit the shape returns
+ * SGEMM_ERR_UNSUPPORTED_SHAPE; one with split_k > 1 needs scratch (sgemm_init). */
+sgemm_status_t sgemm_bf16_skinny_ex(const sgemm_bf16_t *x, long long ldx, const sgemm_bf16_t *W,
+                                    sgemm_bf16_t *y, long long ldy, int M, int N, int K,
+                                    const sgemm_plan_t *plan, sgemm_stream_t stream);
+
+/* One independent problem of a batched call.  ldx / ldy are row strides in
+ * elements, so x may be a strided view (vLLM PR #57617, Controlled follow-up:
+ * the paired inputs are a narrow -> unflatten -> transpose view). */
+typedef struct {
+    const sgemm_bf16_t *x;
+    const sgemm_bf16_t *W;
+    sgemm_bf16_t *y;
+    long long ldx;
+    long long ldy;
+} sgemm_pair_t;
+
+#define SGEMM_MAX_BATCH 8
+
+/* `batch` (1..SGEMM_MAX_BATCH) independent GEMMs of one shape (M, N, K) in ONE
+ * kernel launch: y_i = x_i . W_i^T.  This is the paired f_b_proj / g_b_proj
+ * projection of vLLM PR #57617 (Purpose and source; Microbenchmark table: two
+ * launches become one).  `items` is HOST memory, read during the call only
+ * (its contents travel as kernel parameters, so the call is graph-capturable).
+ * Each item's outputs are bitwise equal to a separate sgemm_bf16_skinny_ex call
+ * with the same plan. */
+sgemm_status_t sgemm_bf16_skinny_batched(const sgemm_pair_t *items, int batch, int M, int N, int K,
+                                         sgemm_stream_t stream);
+
+/* Same, with an explicit plan (NULL = sgemm_plan_select(N, K, M)). */
+sgemm_status_t sgemm_bf16_skinny_batched_ex(const sgemm_pair_t *items, int batch, int M, int N,
+                                            int K, const sgemm_plan_t *plan,
+                                            sgemm_stream_t stream);
+
+/* The plan used for (N, K, M): the entry of the compiled sm_103 plan table
+ * (filled by the offline sweep under CUDA-graph replay with cold L2, as in
+ * vLLM PR #62949, Details, and PR #65306, Details) when it holds one, else a
+ * heuristic plan (id = -1).  Pure host function; never fails (arguments out
+ * of range give the heuristic plan). */
+sgemm_plan_t sgemm_plan_select(int N, int K, int M);
+
+/* Enumerate the compiled kernel configurations (for sweeps and tests):
+ * sgemm_plan_count() of them, index 0..count-1; split_k and ctas_per_sm of a
+ * returned plan may be changed freely before use.  Returns SGEMM_ERR_INVALID_ARG
+ * for an index out of range. */
+int sgemm_plan_count(void);
+sgemm_status_t sgemm_plan_get(int index, sgemm_plan_t *plan);
+
+/* Whether `plan` can run (M, N, K): SGEMM_OK or the status a call would return. */
+sgemm_status_t sgemm_plan_check(const sgemm_plan_t *plan, int M, int N, int K);
+
+/* Allocate the split-K scratch for the current device (idempotent; about
+ * 16 MiB of device memory, kept until process exit).  Calls with a split-K
+ * plan do this themselves on first use, but a first use inside stream capture
+ * cannot allocate and returns SGEMM_ERR_NO_WORKSPACE: call sgemm_init (or run
+ * one call eagerly) before capturing.  Split-K calls on one device share this
+ * scratch, so split-K calls that may run at the same time on different
+ * streams must be ordered by the caller. */
+sgemm_status_t sgemm_init(void);
+
+/* Static description of a status code (never NULL). */
+const char *sgemm_status_string(sgemm_status_t status);
+
+/* Library version, "major.minor.patch". */
+const char *sgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_SKINNY_H */

@@ -1,0 +1,147 @@
+"""The C-ABI library on a CPU-only machine: it loads, exports every function
+the public header declares, and its host-side logic (argument checks, plan
+selection and plan checks) behaves as documented.  No kernel is launched:
+every call below returns before the library touches a CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import bf16_skinny_gemm_gb300 as sk
+from bf16_skinny_gemm_gb300 import build as skbuild
+
+HEADER = os.path.join(skbuild.INCLUDE, "sgemm_skinny.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    skbuild.build()
+    return sk.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(sgemm_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("sgemm_bf16_skinny", "sgemm_bf16_skinny_batched", "sgemm_plan_select"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert sk.sgemm_status_string(s)
+    assert sk.sgemm_status_string(99) == "unknown status"
+    assert re.match(r"^\d+\.\d+\.\d+$", sk.sgemm_version())
+
+
+# pointers that are never dereferenced: every call below fails validation first
+A16 = 0x10000
+NULL = None
+
+
+def _call(lib, x, W, y, M, N, K, ldx=None, ldy=None):
+    return lib.sgemm_bf16_skinny_ex(x, K if ldx is None else ldx, W, y, N if ldy is None else ldy,
+                                    M, N, K, None, None)
+
+
+@pytest.mark.parametrize("M,N,K,expect", [
+    (0, 16, 64, sk.SGEMM_ERR_INVALID_ARG),
+    (5, 16, 64, sk.SGEMM_ERR_INVALID_ARG),
+    (1, 0, 64, sk.SGEMM_ERR_INVALID_ARG),
+    (1, 16, 0, sk.SGEMM_ERR_INVALID_ARG),
+    (1, 16, 12, sk.SGEMM_ERR_UNSUPPORTED_SHAPE),
+    (4, 16, 1001, sk.SGEMM_ERR_UNSUPPORTED_SHAPE),
+])
+def test_bad_shapes_rejected(lib, M, N, K, expect):
+    assert _call(lib, A16, A16, A16, M, N, K) == expect
+
+
+def test_null_pointers_rejected(lib):
+    assert _call(lib, NULL, A16, A16, 1, 16, 64) == sk.SGEMM_ERR_INVALID_ARG
+    assert _call(lib, A16, NULL, A16, 1, 16, 64) == sk.SGEMM_ERR_INVALID_ARG
+    assert _call(lib, A16, A16, NULL, 1, 16, 64) == sk.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_bf16_skinny(A16, A16, NULL, 1, 16, 64, None) == sk.SGEMM_ERR_INVALID_ARG
+
+
+def test_bad_strides_and_alignment_rejected(lib):
+    assert _call(lib, A16, A16, A16, 2, 16, 64, ldx=56) == sk.SGEMM_ERR_INVALID_ARG
+    assert _call(lib, A16, A16, A16, 2, 16, 64, ldy=15) == sk.SGEMM_ERR_INVALID_ARG
+    assert _call(lib, A16, A16, A16, 2, 16, 64, ldx=68) == sk.SGEMM_ERR_MISALIGNED
+    assert _call(lib, A16 + 8, A16, A16, 1, 16, 64) == sk.SGEMM_ERR_MISALIGNED
+    assert _call(lib, A16, A16 + 2, A16, 1, 16, 64) == sk.SGEMM_ERR_MISALIGNED
+    assert _call(lib, A16, A16, A16 + 1, 1, 16, 64) == sk.SGEMM_ERR_MISALIGNED
+
+
+def test_batched_argument_checks(lib):
+    pairs = (sk.Pair * 9)()
+    for p in pairs:
+        p.x, p.W, p.y, p.ldx, p.ldy = A16, A16, A16, 64, 16
+    assert lib.sgemm_bf16_skinny_batched(pairs, 0, 1, 16, 64, None) == sk.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_bf16_skinny_batched(pairs, 9, 1, 16, 64, None) == sk.SGEMM_ERR_INVALID_ARG
+    assert lib.sgemm_bf16_skinny_batched(None, 2, 1, 16, 64, None) == sk.SGEMM_ERR_INVALID_ARG
+    pairs[1].W = A16 + 4
+    assert lib.sgemm_bf16_skinny_batched(pairs, 2, 1, 16, 64, None) == sk.SGEMM_ERR_MISALIGNED
+
+
+def test_bad_plans_rejected(lib):
+    good = sk.sgemm_plan_select(4096, 4096, 1)
+    assert sk.sgemm_plan_check(good, 1, 4096, 4096) == sk.SGEMM_OK
+    for change in ({"variant": 7}, {"threads": 48}, {"threads": 512}, {"vec_bytes": 8},
+                   {"split_k": 0}, {"k_unroll": 3}, {"lanes_per_row": 4}, {"stages": 2}):
+        bad = good.copy(**change)
+        assert sk.sgemm_plan_check(bad, 1, 4096, 4096) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE, change
+        assert _call_plan(lib, bad) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE, change
+    # more splits than chunks of K
+    assert sk.sgemm_plan_check(good.copy(split_k=9), 1, 16, 64) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE
+
+
+def _call_plan(lib, plan):
+    return lib.sgemm_bf16_skinny_ex(A16, 4096, A16, A16, 4096, 1, 4096, 4096,
+                                    ctypes.byref(plan), None)
+
+
+def test_plan_enumeration(lib):
+    n = sk.sgemm_plan_count()
+    assert n >= 8
+    seen = set()
+    for i in range(n):
+        p = sk.sgemm_plan_get(i)
+        key = tuple(p.as_dict().items())
+        assert key not in seen
+        seen.add(key)
+        for M in (1, 2, 3, 4):
+            assert sk.sgemm_plan_check(p, M, 4096, 4096) == sk.SGEMM_OK, p
+    with pytest.raises(sk.SgemmError):
+        sk.sgemm_plan_get(n)
+
+
+SHAPES = [(12576, 4096), (4096, 4096), (2048, 4096), (4096, 1024), (8192, 1536), (4096, 8192),
+          (77440, 4096), (4096, 128), (1, 8), (300, 100000)]
+
+
+@pytest.mark.parametrize("N,K", SHAPES)
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+def test_selected_plans_are_runnable(lib, N, K, M):
+    p = sk.sgemm_plan_select(N, K, M)
+    assert sk.sgemm_plan_check(p, M, N, K) == sk.SGEMM_OK, p
+    # deterministic selection
+    assert p.as_dict() == sk.sgemm_plan_select(N, K, M).as_dict()
+
+
+def test_plan_select_out_of_range_still_returns_a_plan(lib):
+    p = sk.sgemm_plan_select(-1, -1, 9)
+    assert p.threads > 0 and p.id == -1

@@ -63,8 +63,13 @@ def abs_dot(x_bits: np.ndarray, W_bits: np.ndarray) -> np.ndarray:
     return (xa @ wa.T).numpy()
 
 
-def compare(y_gpu_bits, y_ref_bits, x_bits, W_bits, *, tight: bool = True) -> dict:
-    """Check one GEMM result; returns a report dict with ``ok`` and the worst cases."""
+def compare(y_gpu_bits, y_ref_bits, x_bits, W_bits, *, tight: bool = True,
+            cosine: bool = True) -> dict:
+    """Check one GEMM result; returns a report dict with ``ok`` and the worst cases.
+
+    ``cosine=False`` drops the per-row cosine from ``ok``; only hand-made cases
+    whose exact sum is lost to any FP32 accumulation (catastrophic
+    cancellation of terms 2^100 apart) use it."""
     y_gpu_bits = np.asarray(y_gpu_bits, dtype=np.uint16)
     y_ref_bits = np.asarray(y_ref_bits, dtype=np.uint16)
     g = bits_to_f64(y_gpu_bits)
@@ -85,7 +90,8 @@ def compare(y_gpu_bits, y_ref_bits, x_bits, W_bits, *, tight: bool = True) -> di
     bad_kind |= ref_fin & ~np.isfinite(g)
     rep["bad_kind"] = int(bad_kind.sum())
 
-    diff = np.where(ref_fin & np.isfinite(g), np.abs(g - r), 0.0)
+    with np.errstate(invalid="ignore"):
+        diff = np.where(ref_fin & np.isfinite(g), np.abs(g - r), 0.0)
     ns_tol = 2.0 * ulp_bf16(r) + 1e-3 * np.sqrt(K) * max_x * max_w
     ns_bad = ref_fin & (diff > ns_tol)
     rep["ns_violations"] = int(ns_bad.sum())
@@ -122,5 +128,5 @@ def compare(y_gpu_bits, y_ref_bits, x_bits, W_bits, *, tight: bool = True) -> di
     rep["cosine_min"] = cos_min
 
     rep["ok"] = bool(rep["bad_kind"] == 0 and not ns_bad.any() and not t_bad.any()
-                     and cos_min >= 0.99999)
+                     and (cos_min >= 0.99999 or not cosine))
     return rep
