@@ -23,6 +23,7 @@ __all__ = [
     "sgemm_bf16_skinny", "sgemm_bf16_skinny_ex", "sgemm_bf16_skinny_batched",
     "sgemm_bf16_skinny_batched_ex", "sgemm_plan_select", "sgemm_plan_count", "sgemm_plan_get",
     "sgemm_plan_check", "sgemm_init", "sgemm_status_string", "sgemm_version",
+    "sgemm_bf16_skinny_splitk_noalloc", "NOALLOC_SCRATCH_BYTES",
     "SGEMM_OK", "SGEMM_ERR_INVALID_ARG", "SGEMM_ERR_UNSUPPORTED_SHAPE", "SGEMM_ERR_MISALIGNED",
     "SGEMM_ERR_UNSUPPORTED_DEVICE", "SGEMM_ERR_NO_WORKSPACE", "SGEMM_ERR_CUDA", "MAX_BATCH",
 ]
@@ -112,6 +113,8 @@ def load() -> ctypes.CDLL:
         lib.sgemm_init.restype = ci
         lib.sgemm_status_string.argtypes = [ci]
         lib.sgemm_status_string.restype = ctypes.c_char_p
+        lib.sgemm_bf16_skinny_splitk_noalloc.argtypes = [vp, ll, vp, vp, ll, ci, ci, ci, ci, vp]
+        lib.sgemm_bf16_skinny_splitk_noalloc.restype = ci
         lib.sgemm_version.argtypes = []
         lib.sgemm_version.restype = ctypes.c_char_p
         _lib = lib
@@ -216,6 +219,38 @@ def sgemm_bf16_skinny_batched_ex(items, plan: Plan | None = None, stream=None) -
                                                ctypes.byref(plan) if plan is not None else None,
                                                _stream(stream)), "sgemm_bf16_skinny_batched_ex")
     return outs
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def sgemm_bf16_skinny_splitk_noalloc(x: torch.Tensor, W: torch.Tensor,
+                                     y: torch.Tensor | None = None, split_k: int = 2,
+                                     stream=None) -> torch.Tensor:
+    """Split-K ``y = x @ W.T`` that allocates nothing on the device.
+
+    For callers that may not allocate device memory when they run the GEMM
+    (a memory manager that owns the GPU's memory, a plugin with a fixed
+    footprint, a loop where a synchronizing allocation is not allowed).  The
+    partial sums live in a fixed 4 MiB array inside the library, shared by all
+    calls on a device: calls that overlap on the GPU race, and the first call
+    on a device (which looks the array up) should come before stream capture.
+    ``y`` must be given for the call itself to allocate nothing (otherwise this
+    wrapper creates it with torch).  Results equal ``sgemm_bf16_skinny_ex`` with
+    the same split.
+    """
+    M, N, K, y = _problem(x, W, y)
+    need = int(split_k) * M * N * 4
+    if need > NOALLOC_SCRATCH_BYTES:
+        raise SgemmError(SGEMM_ERR_UNSUPPORTED_SHAPE,
+                         f"sgemm_bf16_skinny_splitk_noalloc: split_k*M*N*4 = {need} bytes of "
+                         f"partial sums exceed the fixed {NOALLOC_SCRATCH_BYTES}-byte scratch")
+    ldx = x.stride(0) if M > 1 else K
+    ldy = y.stride(0) if M > 1 else N
+    _check(load().sgemm_bf16_skinny_splitk_noalloc(x.data_ptr(), ldx, W.data_ptr(), y.data_ptr(),
+                                                   ldy, M, N, K, int(split_k), _stream(stream)),
+           "sgemm_bf16_skinny_splitk_noalloc")
+    return y
 
 
 def sgemm_plan_select(N: int, K: int, M: int) -> Plan:

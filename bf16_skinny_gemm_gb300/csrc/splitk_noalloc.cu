@@ -1,0 +1,174 @@
+// Split-K skinny GEMM whose scratch is a fixed array in device memory, so a
+// call allocates nothing.
+//
+// Why it exists: some callers cannot call cudaMalloc (or any allocating
+// routine) at the point where they run a GEMM -- for example code that runs
+// under a memory manager that owns all device memory and forbids other
+// allocations, plugins and embedded runtimes that are not allowed to grow
+// their footprint after start-up, or latency-critical loops where a
+// cudaMalloc (which may synchronize the device) is not acceptable.  The
+// regular split-K path allocates its scratch on first use; this entry point
+// instead uses the file-scope array below, which is part of the library's
+// device image and is created when the library's code is loaded on a device.
+//
+// The kernels are the regular ones (skinny_ldg_kernel with gridDim.y splits,
+// then splitk_reduce_kernel); only where the FP32 partial sums live differs,
+// so results are bitwise equal to sgemm_bf16_skinny_ex with the same plan.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace {
+
+constexpr size_t kScratchFloats = SGEMM_NOALLOC_SCRATCH_BYTES / sizeof(float);
+
+// Shared by every call of sgemm_bf16_skinny_splitk_noalloc on a device; it keeps
+// whatever the last call left in it.  Held by every GPU that loads the library
+// until the process exits.
+static __device__ __align__(256) float g_splitk_scratch[kScratchFloats];
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceSetup {
+    bool done = false;
+    bool supported = false;
+    int sms = 0;
+    float *scratch = nullptr;  // device address of g_splitk_scratch on this device
+};
+
+std::mutex g_mu;
+DeviceSetup g_dev[kMaxDevices];
+
+const sk::KernelInfo *find(int M, const sgemm_plan_t &p) {
+    const sk::KernelInfo *t = nullptr;
+    switch (M) {
+        case 1: t = sk::kKernelsM1; break;
+        case 2: t = sk::kKernelsM2; break;
+        case 3: t = sk::kKernelsM3; break;
+        case 4: t = sk::kKernelsM4; break;
+        default: return nullptr;
+    }
+    for (int i = 0; i < sk::kKernelCountPerM; ++i)
+        if (t[i].variant == p.variant && t[i].R == p.rows_per_warp &&
+            t[i].LPR == p.lanes_per_row && t[i].U == p.k_unroll)
+            return &t[i];
+    return nullptr;
+}
+
+// Once per device, with that device current: look up the array's device
+// address (the host-side name g_splitk_scratch is only a stand-in and must
+// never be handed to a kernel) and allow the kernels their shared memory.
+sgemm_status_t setup_current_device(DeviceSetup **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceSetup &st = g_dev[dev];
+    if (!st.done) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SGEMM_ERR_CUDA;
+        st.supported = (major == 10 && minor == 3);
+        st.sms = sms;
+        if (st.supported) {
+            void *ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_splitk_scratch) != cudaSuccess || ptr == nullptr)
+                return SGEMM_ERR_CUDA;
+            st.scratch = static_cast<float *>(ptr);
+            const sk::KernelInfo *tables[] = {sk::kKernelsM1, sk::kKernelsM2, sk::kKernelsM3,
+                                              sk::kKernelsM4};
+            for (const sk::KernelInfo *t : tables)
+                for (int i = 0; i < sk::kKernelCountPerM; ++i)
+                    if (cudaFuncSetAttribute(t[i].fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             227 * 1024) != cudaSuccess)
+                        return SGEMM_ERR_CUDA;
+        }
+        st.done = true;
+    }
+    if (!st.supported) return SGEMM_ERR_UNSUPPORTED_DEVICE;
+    *out = &st;
+    return SGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" sgemm_status_t sgemm_bf16_skinny_splitk_noalloc(
+    const sgemm_bf16_t *x, long long ldx, const sgemm_bf16_t *W, sgemm_bf16_t *y, long long ldy,
+    int M, int N, int K, int split_k, sgemm_stream_t stream) {
+    if (M < 1 || M > sk::kMaxM || N < 1 || K < 1) return SGEMM_ERR_INVALID_ARG;
+    if (!x || !W || !y || ldx < K || ldy < N) return SGEMM_ERR_INVALID_ARG;
+    if (split_k < 2) return SGEMM_ERR_INVALID_ARG;
+    if (K % 8) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(W)) & 15u)
+        return SGEMM_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(y) & 1u) || ldx % 8) return SGEMM_ERR_MISALIGNED;
+    // the partial sums [split][M][N] must fit the fixed scratch
+    if (static_cast<unsigned long long>(split_k) * M * N > kScratchFloats)
+        return SGEMM_ERR_UNSUPPORTED_SHAPE;
+
+    sgemm_plan_t plan = sgemm_plan_select(N, K, M);
+    plan.split_k = split_k;
+    sgemm_status_t s = sgemm_plan_check(&plan, M, N, K);
+    if (s != SGEMM_OK) return s;
+    const sk::KernelInfo *ki = find(M, plan);
+    if (!ki) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+
+    DeviceSetup *st = nullptr;
+    s = setup_current_device(&st);
+    if (s != SGEMM_OK) return s;
+
+    const int chunks = K / 8;
+    const int kps = (chunks + split_k - 1) / split_k * 8;
+    const size_t smem = static_cast<size_t>(M) * kps * 2;
+
+    sk::Params prm = {};
+    prm.item[0].x = x;
+    prm.item[0].W = W;
+    prm.item[0].y = y;
+    prm.item[0].ldx = ldx;
+    prm.item[0].ldy = ldy;
+    prm.ws = st->scratch;  // every slot the reduce reads is written earlier in this call
+    prm.N = N;
+    prm.K = K;
+    prm.kps = kps;
+    prm.split = split_k;
+    const int rows_per_task = (32 / plan.lanes_per_row) * plan.rows_per_warp;
+    prm.row_groups = (N + rows_per_task - 1) / rows_per_task;
+
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, ki->fn, plan.threads, smem) !=
+            cudaSuccess ||
+        occ < 1)
+        occ = 1;
+    const int warps = plan.threads / 32;
+    const long long need = (prm.row_groups + warps - 1) / warps;
+    long long slots = static_cast<long long>(st->sms) * occ / split_k;
+    if (slots < 1) slots = 1;
+    const int grid_x = static_cast<int>(need < slots ? need : slots);
+
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_x), static_cast<unsigned>(split_k), 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(plan.threads), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = cs;
+    void *args[] = {&prm};
+    if (cudaLaunchKernelExC(&cfg, ki->fn, args) != cudaSuccess) return SGEMM_ERR_CUDA;
+
+    const long long total = static_cast<long long>(M) * N;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 8LL * st->sms) blocks = 8LL * st->sms;
+    cudaLaunchConfig_t rc = {};
+    rc.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    rc.blockDim = dim3(256, 1, 1);
+    rc.stream = cs;
+    int batch = 1;
+    void *rargs[] = {&prm, &batch};
+    if (cudaLaunchKernelExC(&rc, sk::kReduceKernels[M], rargs) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
+    return SGEMM_OK;
+}

@@ -155,6 +155,36 @@ sgemm_status_t sgemm_plan_check(const sgemm_plan_t *plan, int M, int N, int K);
  * streams must be ordered by the caller. */
 sgemm_status_t sgemm_init(void);
 
+/* Size of the fixed device array used by sgemm_bf16_skinny_splitk_noalloc. */
+#define SGEMM_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* Split-K GEMM that allocates nothing.  The paper has no counterpart: this
+ * entry point exists for callers that cannot allocate device memory when they
+ * run the GEMM (code under a memory manager that owns all device memory,
+ * plugins or embedded runtimes that may not grow their footprint after
+ * start-up, latency-critical loops where a possibly synchronizing cudaMalloc
+ * is not allowed).  It computes y = x . W^T exactly like sgemm_bf16_skinny_ex
+ * with the selected plan and split_k splits (bitwise-equal results), but keeps
+ * the FP32 partial sums in a fixed, library-owned device array of
+ * SGEMM_NOALLOC_SCRATCH_BYTES (4 MiB) instead of allocated scratch.
+ * - The caller passes inputs and outputs as for sgemm_bf16_skinny_ex (device
+ *   pointers, strides in elements); split_k must be >= 2.
+ * - split_k * M * N * 4 bytes must fit SGEMM_NOALLOC_SCRATCH_BYTES; larger
+ *   problems return SGEMM_ERR_UNSUPPORTED_SHAPE and launch nothing.
+ * - The first call on a device does a one-time set-up with that device current
+ *   (it looks up the array's device address and sets kernel attributes).
+ *   Make that first call before any stream capture.
+ * - The array lives in every GPU that loads the library until the process
+ *   exits.  All calls on a device share it and it keeps what the last call
+ *   left; nothing in it needs clearing, because each call writes every partial
+ *   sum it later reads.  Calls that overlap on the GPU (other streams,
+ *   concurrent graph launches) race on it: order them.
+ * - Never calls cudaMalloc, cudaFree or any allocating routine. */
+sgemm_status_t sgemm_bf16_skinny_splitk_noalloc(const sgemm_bf16_t *x, long long ldx,
+                                                const sgemm_bf16_t *W, sgemm_bf16_t *y,
+                                                long long ldy, int M, int N, int K, int split_k,
+                                                sgemm_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 const char *sgemm_status_string(sgemm_status_t status);
 
