@@ -223,7 +223,7 @@ class GraphSet:
             yo += R * M * N
             plan = sk.sgemm_plan_select(N, K, M)
             self.cases.append({"N": N, "K": K, "M": M, "R": R, "x": xs, "y": ys, "plan": plan,
-                               "graph": None})
+                               "graphs": {}})
         self.x_host = torch.empty(x_elems, dtype=torch.bfloat16, pin_memory=True)
         self.y_host = torch.empty(y_elems, dtype=torch.bfloat16, pin_memory=True)
         self.x_host.copy_(self.x_pack.cpu())
@@ -231,37 +231,41 @@ class GraphSet:
     def launches_per_step(self):
         return sum(c["R"] * (2 if c["plan"].split_k > 1 else 1) for c in self.cases)
 
-    def capture(self):
+    def capture(self, flags_list):
+        """One graph per (case, launch flags); the GEMMs go through the public
+        sgemm_bf16_skinny_ex call with the selected plan."""
         torch, sk = self.torch, self.sk
         for c in self.cases:  # eager pass first (allocates split-K scratch outside capture)
             W = self.weights[(c["N"], c["K"])]
             for i in range(c["R"]):
-                sk.sgemm_bf16_skinny(c["x"][i], W[i], c["y"][i])
+                sk.sgemm_bf16_skinny_ex(c["x"][i], W[i], c["y"][i], plan=c["plan"])
         torch.cuda.synchronize()
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
-        for c in self.cases:
-            W = self.weights[(c["N"], c["K"])]
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(s):
-                with torch.cuda.graph(g, stream=s):
-                    for i in range(c["R"]):
-                        sk.sgemm_bf16_skinny(c["x"][i], W[i], c["y"][i])
-            c["graph"] = g
+        for flags in flags_list:
+            for c in self.cases:
+                W = self.weights[(c["N"], c["K"])]
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(s):
+                    with torch.cuda.graph(g, stream=s):
+                        for i in range(c["R"]):
+                            sk.sgemm_bf16_skinny_ex(c["x"][i], W[i], c["y"][i], plan=c["plan"],
+                                                    flags=flags)
+                c["graphs"][flags] = g
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
 
     def bytes_per_step(self):
         return sum(c["R"] * gemm_bytes(c["M"], c["N"], c["K"]) for c in self.cases)
 
-    def run_step(self, events=None):
+    def run_step(self, flags, events=None):
         for j, c in enumerate(self.cases):
-            c["graph"].replay()
+            c["graphs"][flags].replay()
             if events is not None:
                 events[j + 1].record()
 
 
-def time_steps(torch, dist, gs, steps, warmup, e2e=False, sampler=None):
+def time_steps(torch, dist, gs, steps, warmup, flags, e2e=False, sampler=None):
     """Run warm-up then exactly `steps` timed steps; returns (max-over-ranks
     seconds, per-case per-step durations in ms)."""
     nc = len(gs.cases)
@@ -269,7 +273,7 @@ def time_steps(torch, dist, gs, steps, warmup, e2e=False, sampler=None):
     def one(events=None):
         if e2e:  # the step's inputs come from pinned host memory, its outputs go back
             gs.x_pack.copy_(gs.x_host, non_blocking=True)
-        gs.run_step(events)
+        gs.run_step(flags, events)
         if e2e:
             gs.y_host.copy_(gs.y_pack, non_blocking=True)
 
@@ -396,6 +400,8 @@ def sweep_config_desc(gs):
          "l2": "inputs larger than L2: each GEMM reads its own weight copy; copies per shape "
                "total >= max(1 GiB, 4 x L2)",
          "timing": "CUDA graph per (N,K,M) of R GEMMs on R copies; CUDA events per graph",
+         "launch": "sgemm_bf16_skinny_ex with the selected plan; the timed chains use the launch "
+                   "flags in 'launch_flags' (weights are never written inside the chain)",
          "parallelism": "replicas"}
     if gs is not None:
         d["copies"] = {f"{c['N']}x{c['K']}": c["R"] for c in gs.cases if c["M"] == 1}
@@ -405,7 +411,7 @@ def sweep_config_desc(gs):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["sweep", "single", "lmhead", "pairs", "chain"],
@@ -415,6 +421,13 @@ def main():
     ap.add_argument("--min-bytes", type=float, default=float(1 << 30),
                     help="weight bytes per (N,K) rotation set (at least 4 x L2 is enforced)")
     ap.add_argument("--reference-rows", type=int, default=32)
+    ap.add_argument("--shapes", default=None,
+                    help="override the sweep shapes, e.g. 12576x4096,4096x1024 (profiling runs)")
+    ap.add_argument("--ms", default=None, help="override the sweep M values, e.g. 1,4")
+    ap.add_argument("--flags", default="pdl,readonly",
+                    help="launch flags of the timed chains: comma list of pdl, readonly, or none")
+    ap.add_argument("--no-plain", action="store_true",
+                    help="skip the extra timing of plain launches (no launch flags)")
     ap.add_argument("--detail-out", default=None, help="also write the full result JSON here")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -441,7 +454,11 @@ def main():
     min_bytes = max(args.min_bytes, 4 * l2)
 
     if args.workload == "sweep":
-        cases = [(N, K, M) for (N, K) in SWEEP_SHAPES for M in SWEEP_MS]
+        shapes = SWEEP_SHAPES
+        if args.shapes:
+            shapes = [tuple(int(v) for v in t.split("x")) for t in args.shapes.split(",")]
+        ms = [int(v) for v in args.ms.split(",")] if args.ms else SWEEP_MS
+        cases = [(N, K, M) for (N, K) in shapes for M in ms]
     elif args.workload == "single":
         cases = [(4096, 1024, 1)]
     elif args.workload == "lmhead":
@@ -449,13 +466,21 @@ def main():
     else:
         raise SystemExit(f"workload {args.workload!r} is not available yet")
 
+    flags = 0
+    for f in args.flags.split(","):
+        flags |= {"pdl": sk.SGEMM_FLAG_PDL, "readonly": sk.SGEMM_FLAG_WEIGHTS_READONLY,
+                  "none": 0}[f.strip()]
+    flag_sets = [flags] if (args.no_plain or flags == 0) else [flags, 0]
     gs = GraphSet(torch, sk, synth, cases, min_bytes, seed=0)
-    gs.capture()
+    gs.capture(flag_sets)
     peak, peak_src = measured_peaks()
 
     sampler = ClockSampler(local) if rank == 0 else None
-    total_s, per_case, clocks = time_steps(torch, dist, gs, args.steps, args.warmup,
+    total_s, per_case, clocks = time_steps(torch, dist, gs, args.steps, args.warmup, flags,
                                            sampler=sampler)
+    plain_case = None
+    if len(flag_sets) > 1:
+        _, plain_case, _ = time_steps(torch, dist, gs, args.steps, args.warmup, 0)
     step_bytes = gs.bytes_per_step()
     all_bytes = dist.sum(step_bytes * args.steps)
     value = all_bytes / total_s / 1e9
@@ -463,13 +488,18 @@ def main():
     detail, kern_bytes, kern_ms = [], 0, 0.0
     traffic, traffic_src = recorded_traffic()
     traffic_sum, traffic_cnt = 0.0, 0
-    for c, ms in zip(gs.cases, per_case):
+    for ci, (c, ms) in enumerate(zip(gs.cases, per_case)):
         med = statistics.median(ms)
         us = med * 1e3 / c["R"]
         b = gemm_bytes(c["M"], c["N"], c["K"])
+        extra = {}
+        if plain_case is not None:
+            us_plain = statistics.median(plain_case[ci]) * 1e3 / c["R"]
+            extra = {"us_plain_launch": round(us_plain, 3),
+                     "gbs_plain_launch": round(b / us_plain / 1e3, 1)}
         detail.append({"N": c["N"], "K": c["K"], "M": c["M"], "copies": c["R"],
                        "us": round(us, 3), "gbs": round(b / us / 1e3, 1),
-                       "frac": round(b / us / 1e3 / peak, 4),
+                       "frac": round(b / us / 1e3 / peak, 4), **extra,
                        "plan": {k: v for k, v in c["plan"].as_dict().items()
                                 if k in ("threads", "rows_per_warp", "lanes_per_row", "k_unroll",
                                          "split_k", "id")}})
@@ -480,8 +510,9 @@ def main():
             traffic_sum += traffic[key]
             traffic_cnt += 1
     for d in detail:
-        base = next(e for e in detail if e["N"] == d["N"] and e["K"] == d["K"] and e["M"] == 1)
-        d["time_vs_m1"] = round(d["us"] / base["us"], 3)
+        base = [e for e in detail if e["N"] == d["N"] and e["K"] == d["K"] and e["M"] == 1]
+        if base:
+            d["time_vs_m1"] = round(d["us"] / base[0]["us"], 3)
     n_launch = gs.launches_per_step() * args.steps
     achieved = kern_bytes / (kern_ms / 1e3) / 1e9
     launches_timed = sum(c["R"] for c in gs.cases) * args.steps
@@ -495,7 +526,7 @@ def main():
 
     e2e = None
     if not args.no_e2e:
-        e2e_s, _, _ = time_steps(torch, dist, gs, args.steps, args.warmup, e2e=True)
+        e2e_s, _, _ = time_steps(torch, dist, gs, args.steps, args.warmup, flags, e2e=True)
         e2e = {"value": round(all_bytes / e2e_s / 1e9, 1), "unit": "GB/s",
                "h2d_bytes_per_step": gs.x_host.numel() * 2,
                "d2h_bytes_per_step": gs.y_host.numel() * 2}
@@ -509,7 +540,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(total_s / args.steps * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": sweep_config_desc(gs) if args.workload == "sweep" else
+            "config": dict(sweep_config_desc(gs), launch_flags=args.flags) if args.workload == "sweep" else
             {"workload": f"{args.workload}: " + ", ".join(f"M={m} ({n},{k})" for n, k, m in cases),
              "l2": "inputs larger than L2 (rotating weight copies)", "parallelism": "replicas"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_launch,

@@ -26,6 +26,8 @@ __all__ = [
     "sgemm_bf16_skinny_splitk_noalloc", "NOALLOC_SCRATCH_BYTES",
     "SGEMM_OK", "SGEMM_ERR_INVALID_ARG", "SGEMM_ERR_UNSUPPORTED_SHAPE", "SGEMM_ERR_MISALIGNED",
     "SGEMM_ERR_UNSUPPORTED_DEVICE", "SGEMM_ERR_NO_WORKSPACE", "SGEMM_ERR_CUDA", "MAX_BATCH",
+    "SGEMM_VARIANT_LDG", "SGEMM_VARIANT_LDG_MIXFMA", "SGEMM_FLAG_PDL",
+    "SGEMM_FLAG_WEIGHTS_READONLY",
 ]
 
 SGEMM_OK = 0
@@ -36,6 +38,10 @@ SGEMM_ERR_UNSUPPORTED_DEVICE = 4
 SGEMM_ERR_NO_WORKSPACE = 5
 SGEMM_ERR_CUDA = 6
 MAX_BATCH = 8
+SGEMM_VARIANT_LDG = 0
+SGEMM_VARIANT_LDG_MIXFMA = 1
+SGEMM_FLAG_PDL = 1
+SGEMM_FLAG_WEIGHTS_READONLY = 2
 
 
 class Plan(ctypes.Structure):
@@ -93,13 +99,14 @@ def load() -> ctypes.CDLL:
         vp, ll, ci = ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int
         lib.sgemm_bf16_skinny.argtypes = [vp, vp, vp, ci, ci, ci, vp]
         lib.sgemm_bf16_skinny.restype = ci
+        cu = ctypes.c_uint
         lib.sgemm_bf16_skinny_ex.argtypes = [vp, ll, vp, vp, ll, ci, ci, ci,
-                                             ctypes.POINTER(Plan), vp]
+                                             ctypes.POINTER(Plan), cu, vp]
         lib.sgemm_bf16_skinny_ex.restype = ci
         lib.sgemm_bf16_skinny_batched.argtypes = [ctypes.POINTER(Pair), ci, ci, ci, ci, vp]
         lib.sgemm_bf16_skinny_batched.restype = ci
         lib.sgemm_bf16_skinny_batched_ex.argtypes = [ctypes.POINTER(Pair), ci, ci, ci, ci,
-                                                     ctypes.POINTER(Plan), vp]
+                                                     ctypes.POINTER(Plan), cu, vp]
         lib.sgemm_bf16_skinny_batched_ex.restype = ci
         lib.sgemm_plan_select.argtypes = [ci, ci, ci]
         lib.sgemm_plan_select.restype = Plan
@@ -170,14 +177,15 @@ def sgemm_bf16_skinny(x: torch.Tensor, W: torch.Tensor, y: torch.Tensor | None =
 
 
 def sgemm_bf16_skinny_ex(x: torch.Tensor, W: torch.Tensor, y: torch.Tensor | None = None,
-                         plan: Plan | None = None, stream=None) -> torch.Tensor:
-    """Like :func:`sgemm_bf16_skinny` with strided x / y rows and an optional plan."""
+                         plan: Plan | None = None, flags: int = 0, stream=None) -> torch.Tensor:
+    """Like :func:`sgemm_bf16_skinny` with strided x / y rows, an optional plan
+    and launch flags (``SGEMM_FLAG_*``)."""
     M, N, K, y = _problem(x, W, y)
     ldx = x.stride(0) if M > 1 else K
     ldy = y.stride(0) if M > 1 else N
     _check(load().sgemm_bf16_skinny_ex(x.data_ptr(), ldx, W.data_ptr(), y.data_ptr(), ldy,
                                        M, N, K, ctypes.byref(plan) if plan is not None else None,
-                                       _stream(stream)), "sgemm_bf16_skinny_ex")
+                                       int(flags), _stream(stream)), "sgemm_bf16_skinny_ex")
     return y
 
 
@@ -212,12 +220,14 @@ def sgemm_bf16_skinny_batched(items, stream=None) -> list:
     return outs
 
 
-def sgemm_bf16_skinny_batched_ex(items, plan: Plan | None = None, stream=None) -> list:
-    """:func:`sgemm_bf16_skinny_batched` with an explicit plan."""
+def sgemm_bf16_skinny_batched_ex(items, plan: Plan | None = None, flags: int = 0,
+                                 stream=None) -> list:
+    """:func:`sgemm_bf16_skinny_batched` with an explicit plan and launch flags."""
     arr, (M, N, K), outs = _pairs(items)
     _check(load().sgemm_bf16_skinny_batched_ex(arr, len(items), M, N, K,
                                                ctypes.byref(plan) if plan is not None else None,
-                                               _stream(stream)), "sgemm_bf16_skinny_batched_ex")
+                                               int(flags), _stream(stream)),
+           "sgemm_bf16_skinny_batched_ex")
     return outs
 
 

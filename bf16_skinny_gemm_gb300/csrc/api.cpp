@@ -79,7 +79,8 @@ int split_kps(int K, int split) {
 
 sgemm_status_t check_plan(const sgemm_plan_t &p, int M, int N, int K) {
     (void)N;
-    if (p.variant != SGEMM_VARIANT_LDG) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (p.variant != SGEMM_VARIANT_LDG && p.variant != SGEMM_VARIANT_LDG_MIXFMA)
+        return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.threads < 32 || p.threads > sk::kMaxThreads || p.threads % 32) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.vec_bytes != 16 || p.stages != 0) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.split_k < 1 || p.split_k > 64) return SGEMM_ERR_UNSUPPORTED_SHAPE;
@@ -112,9 +113,7 @@ sgemm_plan_t heuristic_plan(int N, int K, int M) {
     (void)N;
     int R, LPR, U;
     if (K <= 128) {
-        R = 2, LPR = 16, U = 1;
-    } else if (K <= 256) {
-        R = 2, LPR = 32, U = 2;
+        R = 2, LPR = 16, U = 2;
     } else if (M <= 2) {
         R = 1, LPR = 32, U = 8;
     } else {
@@ -127,7 +126,7 @@ sgemm_plan_t heuristic_plan(int N, int K, int M) {
         split = static_cast<int>((xbytes + budget - 1) / budget);
         split = std::max(1, std::min(split, 64));
     }
-    return make_plan(SGEMM_VARIANT_LDG, 256, R, LPR, U, split, 0, 0, -1);
+    return make_plan(SGEMM_VARIANT_LDG_MIXFMA, 256, R, LPR, U, split, 0, 0, -1);
 }
 
 sgemm_status_t probe_device(int *dev_out, DeviceState **st_out) {
@@ -204,9 +203,10 @@ sgemm_status_t validate_item(const sgemm_pair_t &it, int N, int K) {
 }
 
 sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
-                   const sgemm_plan_t *plan_in, cudaStream_t stream) {
+                   const sgemm_plan_t *plan_in, unsigned flags, cudaStream_t stream) {
     sgemm_status_t s = validate_common(M, N, K, batch);
     if (s != SGEMM_OK) return s;
+    if (flags & ~(SGEMM_FLAG_PDL | SGEMM_FLAG_WEIGHTS_READONLY)) return SGEMM_ERR_INVALID_ARG;
     if (!items) return SGEMM_ERR_INVALID_ARG;
     for (int b = 0; b < batch; ++b) {
         s = validate_item(items[b], N, K);
@@ -242,6 +242,7 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
     prm.split = split;
     const int rows_per_task = (32 / plan.lanes_per_row) * plan.rows_per_warp;
     prm.row_groups = (N + rows_per_task - 1) / rows_per_task;
+    prm.flags = static_cast<int>(flags);
 
     int grid_x = 0;
     {
@@ -274,6 +275,13 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
     cfg.blockDim = dim3(static_cast<unsigned>(plan.threads), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (flags & SGEMM_FLAG_PDL) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     void *args[] = {&prm};
     if (cudaLaunchKernelExC(&cfg, ki->fn, args) != cudaSuccess) return SGEMM_ERR_CUDA;
 
@@ -286,6 +294,10 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
         rc.blockDim = dim3(256, 1, 1);
         rc.dynamicSmemBytes = 0;
         rc.stream = stream;
+        if (flags & SGEMM_FLAG_PDL) {
+            rc.attrs = attr;
+            rc.numAttrs = 1;
+        }
         int batch_arg = batch;
         void *rargs[] = {&prm, &batch_arg};
         if (cudaLaunchKernelExC(&rc, sk::kReduceKernels[M], rargs) != cudaSuccess)
@@ -329,30 +341,31 @@ sgemm_status_t sgemm_plan_check(const sgemm_plan_t *plan, int M, int N, int K) {
 
 sgemm_status_t sgemm_bf16_skinny_ex(const sgemm_bf16_t *x, long long ldx, const sgemm_bf16_t *W,
                                     sgemm_bf16_t *y, long long ldy, int M, int N, int K,
-                                    const sgemm_plan_t *plan, sgemm_stream_t stream) {
+                                    const sgemm_plan_t *plan, unsigned flags,
+                                    sgemm_stream_t stream) {
     sgemm_pair_t it;
     it.x = x;
     it.W = W;
     it.y = y;
     it.ldx = ldx;
     it.ldy = ldy;
-    return run(&it, 1, M, N, K, plan, reinterpret_cast<cudaStream_t>(stream));
+    return run(&it, 1, M, N, K, plan, flags, reinterpret_cast<cudaStream_t>(stream));
 }
 
 sgemm_status_t sgemm_bf16_skinny(const sgemm_bf16_t *x, const sgemm_bf16_t *W, sgemm_bf16_t *y,
                                  int M, int N, int K, sgemm_stream_t stream) {
-    return sgemm_bf16_skinny_ex(x, K, W, y, N, M, N, K, nullptr, stream);
+    return sgemm_bf16_skinny_ex(x, K, W, y, N, M, N, K, nullptr, 0u, stream);
 }
 
 sgemm_status_t sgemm_bf16_skinny_batched_ex(const sgemm_pair_t *items, int batch, int M, int N,
-                                            int K, const sgemm_plan_t *plan,
+                                            int K, const sgemm_plan_t *plan, unsigned flags,
                                             sgemm_stream_t stream) {
-    return run(items, batch, M, N, K, plan, reinterpret_cast<cudaStream_t>(stream));
+    return run(items, batch, M, N, K, plan, flags, reinterpret_cast<cudaStream_t>(stream));
 }
 
 sgemm_status_t sgemm_bf16_skinny_batched(const sgemm_pair_t *items, int batch, int M, int N, int K,
                                          sgemm_stream_t stream) {
-    return run(items, batch, M, N, K, nullptr, reinterpret_cast<cudaStream_t>(stream));
+    return run(items, batch, M, N, K, nullptr, 0u, reinterpret_cast<cudaStream_t>(stream));
 }
 
 sgemm_status_t sgemm_init(void) {

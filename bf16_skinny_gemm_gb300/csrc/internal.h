@@ -23,6 +23,10 @@ struct Item {
     long long ldy;
 };
 
+// Params::flags bits (the launch flags of the C ABI, SGEMM_FLAG_*).
+constexpr int kFlagPdl = SGEMM_FLAG_PDL;
+constexpr int kFlagWeightsReadOnly = SGEMM_FLAG_WEIGHTS_READONLY;
+
 // Kernel parameters (passed by value; about 350 bytes).
 struct Params {
     Item item[kMaxBatch];
@@ -32,6 +36,7 @@ struct Params {
     int kps;         // K elements per split (a multiple of 8); the last split may be shorter
     int split;       // number of K splits (gridDim.y)
     int row_groups;  // ceil(N / rows per warp task)
+    int flags;       // SGEMM_FLAG_* bits
 };
 
 // A compiled instantiation of a kernel template.

@@ -3,7 +3,7 @@
 
 namespace sk {
 
-#define SK_COUNT_ONE(M, R, LPR, U) +1
+#define SK_COUNT_ONE(M, R, LPR, U, MIX) +1
 const int kKernelCountPerM = 0 SK_LDG_CONFIGS(SK_COUNT_ONE, 1);
 
 const void *const kReduceKernels[kMaxM + 1] = {

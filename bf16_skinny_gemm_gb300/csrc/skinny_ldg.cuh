@@ -8,22 +8,35 @@
 // library GEMM's split-K + reduce).  The design here is our own for GB300:
 //
 //  * W is read exactly once, with 128-bit non-allocating loads
-//    (ld.global.nc.L1::no_allocate), U loads per row per lane in flight so that
-//    enough bytes are outstanding to cover HBM latency.
+//    (ld.global.nc.L1::no_allocate).  Each lane walks a flat sequence of
+//    (row group, K chunk) iterations that runs across row boundaries, issuing
+//    U loads at once and consuming them together.  Batches rather than a
+//    rolling ring: measured on GB300, a register ring of loads consumed one at
+//    a time keeps only about one load per warp in flight, while a batch keeps
+//    all U in flight (5.1 vs 1.3 TB/s at 8 warps per SM).  The number of bytes
+//    in flight therefore does not depend on K.
+//  * The first U loads are issued before x is staged, so the latency of the
+//    W stream and of the x staging overlap.
 //  * x (all M rows of this CTA's K range) is staged once per CTA in shared
 //    memory and re-read from there for every row: it is tiny next to W.
-//  * A warp is split into 32/LPR lane groups; each group owns R rows and walks
-//    their K range with stride LPR chunks of 8 elements.  Each lane keeps M*R
-//    FP32 accumulators; products are exact in FP32 and added with FMA.
+//  * A warp is split into 32/LPR lane groups; each group owns R rows at a time
+//    and walks their K range with stride LPR chunks of 8 elements.  Each lane
+//    keeps M*R FP32 accumulators.  Products are exact in FP32 and are added
+//    with FMA: either after widening both BF16 operands to FP32 (MIX = false)
+//    or with the sm_100+ mixed-precision FMA that takes BF16 operands and an
+//    FP32 addend directly (MIX = true); both round once per addition to FP32.
 //  * Lane partial sums are combined with an xor-butterfly of warp shuffles
 //    (fixed order).  With split-K (gridDim.y > 1) each split writes FP32
 //    partials and a second kernel adds them in split order.
 //  * The grid is sized for the GPU (SMs x resident CTAs) and each CTA takes a
-//    balanced contiguous range of row groups, so every SM streams an equal
-//    share of W.
+//    balanced contiguous range of row groups.
+//  * Optional programmatic dependent launch: the kernel lets the next kernel
+//    on the stream launch early, and waits for the previous one before it
+//    reads x or writes y (and, unless told that W is read-only with respect to
+//    the previous kernel, before it reads W).
 //
 // Accumulation order for one output is a function of (K range, LPR) only: it
-// never depends on M, R, U, the CTA size or the grid, which makes results
+// never depends on M, R, U, MIX, the CTA size or the grid, which makes results
 // deterministic and row-wise independent of M.
 #pragma once
 
@@ -36,11 +49,18 @@ namespace sk {
 // 16 bytes of W, streamed: no L1 allocation, 256-byte L2 prefetch granule.
 __device__ __forceinline__ uint4 ldg_stream(const uint16_t *p) {
     uint4 r;
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
     return r;
 }
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Returns at once when the kernel was not launched as a programmatic dependent.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // BF16 -> FP32 is exact: the BF16 bits are the top half of the FP32 bits.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -50,42 +70,86 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-// acc[m] += sum over the 8 elements of one chunk, in element order.
-template <int M, int R>
-__device__ __forceinline__ void fma_chunk(float (&acc)[M][R], const float (&xf)[M][8],
-                                          const uint4 &w, int r) {
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float w0 = bf16_lo(ww[i]);
-        const float w1 = bf16_hi(ww[i]);
-#pragma unroll
-        for (int m = 0; m < M; ++m) {
-            acc[m][r] = fmaf(xf[m][2 * i], w0, acc[m][r]);
-            acc[m][r] = fmaf(xf[m][2 * i + 1], w1, acc[m][r]);
-        }
-    }
+// acc += lo(x)*lo(w), then acc += hi(x)*hi(w): BF16 operands, FP32 addend,
+// one round-to-nearest per FMA.
+__device__ __forceinline__ float fma2_bf16(uint32_t xw, uint32_t ww, float acc) {
+    asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t"
+        "mov.b32 {xl, xh}, %1;\n\t"
+        "mov.b32 {wl, wh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, xl, wl, %0;\n\t"
+        "fma.rn.f32.bf16 %0, xh, wh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(xw), "r"(ww));
+    return acc;
 }
+
+// x operand of one chunk (8 elements) for all M rows: widened to FP32, or kept
+// as packed BF16 pairs for the mixed-precision FMA.
+template <int M, bool MIX>
+struct XChunk;
 
 template <int M>
-__device__ __forceinline__ void unpack_x(float (&xf)[M][8], const uint4 *xs, int nchunk, int c) {
+struct XChunk<M, false> {
+    float v[M][8];
+    __device__ __forceinline__ void load(const uint4 *xs, int nchunk, int c) {
 #pragma unroll
-    for (int m = 0; m < M; ++m) {
-        const uint4 v = xs[m * nchunk + c];
-        const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+        for (int m = 0; m < M; ++m) {
+            const uint4 q = xs[m * nchunk + c];
+            const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            xf[m][2 * i] = bf16_lo(vv[i]);
-            xf[m][2 * i + 1] = bf16_hi(vv[i]);
+            for (int i = 0; i < 4; ++i) {
+                v[m][2 * i] = bf16_lo(qq[i]);
+                v[m][2 * i + 1] = bf16_hi(qq[i]);
+            }
         }
     }
-}
+    template <int R>
+    __device__ __forceinline__ void fma(float (&acc)[M][R], const uint4 &w, int r) const {
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float w0 = bf16_lo(ww[i]);
+            const float w1 = bf16_hi(ww[i]);
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                acc[m][r] = fmaf(v[m][2 * i], w0, acc[m][r]);
+                acc[m][r] = fmaf(v[m][2 * i + 1], w1, acc[m][r]);
+            }
+        }
+    }
+};
 
-template <int M, int R, int LPR, int U>
+template <int M>
+struct XChunk<M, true> {
+    uint32_t v[M][4];
+    __device__ __forceinline__ void load(const uint4 *xs, int nchunk, int c) {
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            const uint4 q = xs[m * nchunk + c];
+            v[m][0] = q.x;
+            v[m][1] = q.y;
+            v[m][2] = q.z;
+            v[m][3] = q.w;
+        }
+    }
+    template <int R>
+    __device__ __forceinline__ void fma(float (&acc)[M][R], const uint4 &w, int r) const {
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int m = 0; m < M; ++m) acc[m][r] = fma2_bf16(v[m][i], ww[i], acc[m][r]);
+    }
+};
+
+template <int M, int R, int LPR, int U, bool MIX>
 __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_constant__ Params p) {
     static_assert(LPR == 32 || LPR == 16 || LPR == 8, "lanes per row");
     constexpr int G = 32 / LPR;  // lane groups per warp
     extern __shared__ uint4 xs[];  // [M][nchunk] chunks of 8 BF16
+
+    const bool pdl = (p.flags & kFlagPdl) != 0;
+    if (pdl) pdl_launch_dependents();
 
     const Item &it = p.item[blockIdx.z];
     const int s = blockIdx.y;
@@ -93,7 +157,61 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
     const int kc = min(p.K - k0, p.kps);
     const int nchunk = kc >> 3;
 
-    // stage x[:, k0:k0+kc] in shared memory
+    const int warps = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int gi = lane / LPR;  // lane group
+    const int li = lane % LPR;  // lane in group
+
+    // balanced contiguous range of row groups for this CTA; warps interleave
+    const long long RG = p.row_groups;
+    const int g_begin = static_cast<int>(RG * blockIdx.x / gridDim.x);
+    const int g_end = static_cast<int>(RG * (blockIdx.x + 1) / gridDim.x);
+    const int g0 = g_begin + warp;
+    const int ntask = g0 < g_end ? (g_end - g0 + warps - 1) / warps : 0;
+    const int jtot = (nchunk + LPR - 1) / LPR;          // iterations per task
+    const int last_lanes = nchunk - (jtot - 1) * LPR;   // lanes busy in a task's last iteration
+    const int total = ntask * jtot;                     // iterations of this warp
+
+    // Load cursor (task lt, iteration lj) and consume cursor (task ct, iteration cj)
+    // walk the same flat sequence of this warp's iterations.  Loads are issued in
+    // batches of U iterations (which may span tasks) and the whole batch is consumed
+    // before the next batch is issued: every load of a batch is in flight at once.
+    int lt = 0, lj = 0;
+    const uint16_t *lrow[R];
+    auto rows_of = [&](int t) {
+        const int n0 = ((g0 + t * warps) * G + gi) * R;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int n = min(n0 + r, p.N - 1);  // rows past N re-read row N-1; result dropped
+            lrow[r] = it.W + static_cast<long long>(n) * p.K + k0 + 8 * li;
+        }
+    };
+    rows_of(0);
+
+    uint4 buf[U][R];
+    auto issue_batch = [&](int base) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (base + u < total) {
+                const bool ok = (lj < jtot - 1) || (li < last_lanes);
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    buf[u][r] = ok ? ldg_stream(lrow[r] + 8 * LPR * lj) : make_uint4(0u, 0u, 0u, 0u);
+                if (++lj == jtot) {
+                    lj = 0;
+                    if (++lt < ntask) rows_of(lt);
+                }
+            }
+        }
+    };
+
+    const bool early_w = !pdl || (p.flags & kFlagWeightsReadOnly);
+    if (early_w) issue_batch(0);
+    if (pdl) pdl_wait();
+    if (!early_w) issue_batch(0);
+
+    // stage x[:, k0:k0+kc] in shared memory (overlaps the first batch's latency)
     for (int i = threadIdx.x; i < M * nchunk; i += blockDim.x) {
         const int m = i / nchunk;
         const int c = i - m * nchunk;
@@ -101,96 +219,64 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
     }
     __syncthreads();
 
-    const int warps = blockDim.x >> 5;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int gi = lane / LPR;  // lane group
-    const int li = lane % LPR;  // lane in group
+    float acc[M][R];
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int r = 0; r < R; ++r) acc[m][r] = 0.0f;
 
-    // balanced contiguous range of row groups for this CTA
-    const long long RG = p.row_groups;
-    const int g_begin = static_cast<int>(RG * blockIdx.x / gridDim.x);
-    const int g_end = static_cast<int>(RG * (blockIdx.x + 1) / gridDim.x);
-    const int jfull = nchunk / LPR;      // iterations with every lane of the group busy
-    const int rem = nchunk - jfull * LPR;  // chunks of the final partial iteration
-
-    for (int g = g_begin + warp; g < g_end; g += warps) {
-        const int n0 = (g * G + gi) * R;
-        const uint16_t *wr[R];
+    int ct = 0, cj = 0;
+    for (int base = 0; base < total; base += U) {
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int n = min(n0 + r, p.N - 1);  // rows past N re-read row N-1; result dropped
-            wr[r] = it.W + static_cast<long long>(n) * p.K + k0 + 8 * li;
-        }
-        float acc[M][R];
+        for (int u = 0; u < U; ++u) {
+            if (base + u < total) {
+                if ((cj < jtot - 1) || (li < last_lanes)) {
+                    XChunk<M, MIX> xc;
+                    xc.load(xs, nchunk, li + LPR * cj);
 #pragma unroll
-        for (int m = 0; m < M; ++m)
+                    for (int r = 0; r < R; ++r) xc.template fma<R>(acc, buf[u][r], r);
+                }
+                if (++cj == jtot) {
+                    // task done: xor-butterfly over the LPR lanes (fixed tree order)
 #pragma unroll
-            for (int r = 0; r < R; ++r) acc[m][r] = 0.0f;
-
-        int j = 0;
-        for (; j + U <= jfull; j += U) {
-            uint4 w[U][R];
+                    for (int m = 0; m < M; ++m)
 #pragma unroll
-            for (int u = 0; u < U; ++u)
+                        for (int r = 0; r < R; ++r) {
+                            float v = acc[m][r];
 #pragma unroll
-                for (int r = 0; r < R; ++r) w[u][r] = ldg_stream(wr[r] + 8 * LPR * (j + u));
+                            for (int off = LPR / 2; off >= 1; off >>= 1)
+                                v += __shfl_xor_sync(0xffffffffu, v, off);
+                            acc[m][r] = v;
+                        }
+                    if (li == 0) {
+                        const int n0 = ((g0 + ct * warps) * G + gi) * R;
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                float xf[M][8];
-                unpack_x<M>(xf, xs, nchunk, li + LPR * (j + u));
+                        for (int r = 0; r < R; ++r) {
+                            const int n = n0 + r;
+                            if (n < p.N) {
 #pragma unroll
-                for (int r = 0; r < R; ++r) fma_chunk<M, R>(acc, xf, w[u][r], r);
-            }
-        }
-        for (; j < jfull; ++j) {
-            uint4 w[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) w[r] = ldg_stream(wr[r] + 8 * LPR * j);
-            float xf[M][8];
-            unpack_x<M>(xf, xs, nchunk, li + LPR * j);
-#pragma unroll
-            for (int r = 0; r < R; ++r) fma_chunk<M, R>(acc, xf, w[r], r);
-        }
-        if (li < rem) {
-            uint4 w[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) w[r] = ldg_stream(wr[r] + 8 * LPR * jfull);
-            float xf[M][8];
-            unpack_x<M>(xf, xs, nchunk, li + LPR * jfull);
-#pragma unroll
-            for (int r = 0; r < R; ++r) fma_chunk<M, R>(acc, xf, w[r], r);
-        }
-
-        // xor-butterfly over the LPR lanes of the group (fixed tree order)
-#pragma unroll
-        for (int m = 0; m < M; ++m)
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                float v = acc[m][r];
-#pragma unroll
-                for (int off = LPR / 2; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                acc[m][r] = v;
-            }
-
-        if (li == 0) {
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int n = n0 + r;
-                if (n < p.N) {
-#pragma unroll
-                    for (int m = 0; m < M; ++m) {
-                        if (p.split == 1) {
-                            it.y[m * it.ldy + n] = f32_to_bf16_rn(acc[m][r]);
-                        } else {
-                            const long long slot =
-                                ((static_cast<long long>(blockIdx.z) * p.split + s) * M + m);
-                            p.ws[slot * p.N + n] = acc[m][r];
+                                for (int m = 0; m < M; ++m) {
+                                    if (p.split == 1) {
+                                        it.y[m * it.ldy + n] = f32_to_bf16_rn(acc[m][r]);
+                                    } else {
+                                        const long long slot =
+                                            (static_cast<long long>(blockIdx.z) * p.split + s) * M + m;
+                                        p.ws[slot * p.N + n] = acc[m][r];
+                                    }
+                                }
+                            }
                         }
                     }
+#pragma unroll
+                    for (int m = 0; m < M; ++m)
+#pragma unroll
+                        for (int r = 0; r < R; ++r) acc[m][r] = 0.0f;
+                    cj = 0;
+                    ++ct;
                 }
             }
         }
+        if (base + U < total) issue_batch(base + U);
     }
 }
 
@@ -198,6 +284,10 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
 template <int M>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ Params p,
                                                              int batch) {
+    if (p.flags & kFlagPdl) {
+        pdl_launch_dependents();
+        pdl_wait();
+    }
     const long long per_item = static_cast<long long>(M) * p.N;
     const long long total = per_item * batch;
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;

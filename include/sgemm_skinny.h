@@ -86,20 +86,41 @@ typedef struct {
 } sgemm_plan_t;
 
 enum {
-    SGEMM_VARIANT_LDG = 0  /* W streamed with 128-bit non-allocating loads into registers,
-                              x staged in shared memory, warp-shuffle reduction */
+    SGEMM_VARIANT_LDG = 0,        /* W streamed with 128-bit non-allocating loads into a ring of
+                                     registers, x staged in shared memory, BF16 widened to FP32,
+                                     FP32 FMA, warp-shuffle reduction */
+    SGEMM_VARIANT_LDG_MIXFMA = 1  /* the same with the mixed-precision FMA (BF16 operands, FP32
+                                     addend): fewer instructions, bitwise-identical results */
 };
+
+/* Launch flags (bit set) for the _ex calls.
+ * SGEMM_FLAG_PDL: launch as a programmatic dependent of the previous kernel on
+ *   the stream.  The kernel lets the next kernel launch early and waits for
+ *   the previous kernel to finish (and its writes to be visible) before it
+ *   reads x or writes y, so the results are those of a plain launch; the gain
+ *   is that launch latency and the kernel's start-up overlap the previous
+ *   kernel's tail.
+ * SGEMM_FLAG_WEIGHTS_READONLY (with SGEMM_FLAG_PDL): the caller promises that
+ *   W is not written by any work that may still be running on the stream when
+ *   this call is reached (for example decode weights that no kernel of the
+ *   step modifies).  The kernel then starts streaming W before the previous
+ *   kernel finishes. */
+#define SGEMM_FLAG_PDL 1u
+#define SGEMM_FLAG_WEIGHTS_READONLY 2u
 
 /* y = x . W^T for contiguous x [M,K] and y [M,N].  Plan: sgemm_plan_select(N, K, M). */
 sgemm_status_t sgemm_bf16_skinny(const sgemm_bf16_t *x, const sgemm_bf16_t *W, sgemm_bf16_t *y,
                                  int M, int N, int K, sgemm_stream_t stream);
 
-/* As sgemm_bf16_skinny with row strides for x and y and an optional plan
- * (NULL = sgemm_plan_select).  A plan that does not fit the shape returns
- * SGEMM_ERR_UNSUPPORTED_SHAPE; one with split_k > 1 needs scratch (sgemm_init). */
+/* As sgemm_bf16_skinny with row strides for x and y, an optional plan
+ * (NULL = sgemm_plan_select) and launch flags (SGEMM_FLAG_*; 0 = a plain
+ * launch).  A plan that does not fit the shape, or unknown flag bits, return
+ * SGEMM_ERR_UNSUPPORTED_SHAPE / SGEMM_ERR_INVALID_ARG; a plan with
+ * split_k > 1 needs scratch (sgemm_init). */
 sgemm_status_t sgemm_bf16_skinny_ex(const sgemm_bf16_t *x, long long ldx, const sgemm_bf16_t *W,
                                     sgemm_bf16_t *y, long long ldy, int M, int N, int K,
-                                    const sgemm_plan_t *plan, sgemm_stream_t stream);
+                                    const sgemm_plan_t *plan, unsigned flags,
+                                    sgemm_stream_t stream);
 
 /* One independent problem of a batched call.  ldx / ldy are row strides in
  * elements, so x may be a strided view (vLLM PR #57617, Controlled follow-up:
@@ -124,9 +145,10 @@ typedef struct {
 sgemm_status_t sgemm_bf16_skinny_batched(const sgemm_pair_t *items, int batch, int M, int N, int K,
                                          sgemm_stream_t stream);
 
-/* Same, with an explicit plan (NULL = sgemm_plan_select(N, K, M)). */
+/* Same, with an explicit plan (NULL = sgemm_plan_select(N, K, M)) and launch
+ * flags (SGEMM_FLAG_*, as for sgemm_bf16_skinny_ex). */
 sgemm_status_t sgemm_bf16_skinny_batched_ex(const sgemm_pair_t *items, int batch, int M, int N,
-                                            int K, const sgemm_plan_t *plan,
+                                            int K, const sgemm_plan_t *plan, unsigned flags,
                                             sgemm_stream_t stream);
 
 /* The plan used for (N, K, M): the entry of the compiled sm_103 plan table

@@ -55,7 +55,7 @@ NULL = None
 
 def _call(lib, x, W, y, M, N, K, ldx=None, ldy=None):
     return lib.sgemm_bf16_skinny_ex(x, K if ldx is None else ldx, W, y, N if ldy is None else ldy,
-                                    M, N, K, None, None)
+                                    M, N, K, None, 0, None)
 
 
 @pytest.mark.parametrize("M,N,K,expect", [
@@ -86,6 +86,15 @@ def test_bad_strides_and_alignment_rejected(lib):
     assert _call(lib, A16, A16, A16 + 1, 1, 16, 64) == sk.SGEMM_ERR_MISALIGNED
 
 
+def test_unknown_flags_rejected(lib):
+    assert lib.sgemm_bf16_skinny_ex(A16, 64, A16, A16, 16, 1, 16, 64, None, 4, None) == \
+        sk.SGEMM_ERR_INVALID_ARG
+    pairs = (sk.Pair * 1)()
+    pairs[0].x, pairs[0].W, pairs[0].y, pairs[0].ldx, pairs[0].ldy = A16, A16, A16, 64, 16
+    assert lib.sgemm_bf16_skinny_batched_ex(pairs, 1, 1, 16, 64, None, 8, None) == \
+        sk.SGEMM_ERR_INVALID_ARG
+
+
 def test_batched_argument_checks(lib):
     pairs = (sk.Pair * 9)()
     for p in pairs:
@@ -100,7 +109,7 @@ def test_batched_argument_checks(lib):
 def test_bad_plans_rejected(lib):
     good = sk.sgemm_plan_select(4096, 4096, 1)
     assert sk.sgemm_plan_check(good, 1, 4096, 4096) == sk.SGEMM_OK
-    for change in ({"variant": 7}, {"threads": 48}, {"threads": 512}, {"vec_bytes": 8},
+    for change in ({"variant": 7}, {"variant": -1}, {"threads": 48}, {"threads": 512}, {"vec_bytes": 8},
                    {"split_k": 0}, {"k_unroll": 3}, {"lanes_per_row": 4}, {"stages": 2}):
         bad = good.copy(**change)
         assert sk.sgemm_plan_check(bad, 1, 4096, 4096) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE, change
@@ -111,7 +120,7 @@ def test_bad_plans_rejected(lib):
 
 def _call_plan(lib, plan):
     return lib.sgemm_bf16_skinny_ex(A16, 4096, A16, A16, 4096, 1, 4096, 4096,
-                                    ctypes.byref(plan), None)
+                                    ctypes.byref(plan), 0, None)
 
 
 def test_plan_enumeration(lib):

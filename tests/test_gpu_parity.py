@@ -320,3 +320,69 @@ def test_batched_graph_replay():
     torch.cuda.synchronize()
     for it, e in zip(items, eager):
         assert torch.equal(it[2].view(torch.int16), e.view(torch.int16))
+
+
+# ------------------------------------------- plan equivalence and launch flags
+@pytest.mark.parametrize("M", [1, 3, 4])
+def test_plans_with_same_lanes_per_row_agree_bitwise(M):
+    """The accumulation order depends only on (K range, lanes per row): the
+    mixed-precision FMA and the widened FP32 FMA, any R, U and CTA size must
+    give the same bits."""
+    N, K = 1500, 3072
+    x, W = _inputs(M, N, K, seed=31)
+    xd, Wd = x.to(DEV), W.to(DEV)
+    by_lpr = {}
+    for p in _all_plans():
+        for split in (1, 2):
+            plan = p.copy(split_k=split)
+            y = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=plan)
+            torch.cuda.synchronize()
+            key = (plan.lanes_per_row, split)
+            if key in by_lpr:
+                assert torch.equal(by_lpr[key][1].view(torch.int16), y.view(torch.int16)), \
+                    (by_lpr[key][0], plan)
+            else:
+                by_lpr[key] = (plan, y)
+    for (lpr, split), (plan, y) in by_lpr.items():
+        _check(x, W, y)
+
+
+def _chain(xd, Ws, flags, plan_split=1):
+    """y_i = x_i W_i^T where x_{i+1} is a rescaled copy of y_i (a dependent chain)."""
+    outs = []
+    x = xd
+    for W in Ws:
+        N, K = W.shape
+        plan = sk.sgemm_plan_select(N, K, x.shape[0]).copy(split_k=plan_split)
+        y = torch.empty((x.shape[0], N), dtype=torch.bfloat16, device=DEV)
+        sk.sgemm_bf16_skinny_ex(x, W, y, plan=plan, flags=flags)
+        outs.append(y)
+        x = (y[:, :K].float() * 8.0).to(torch.bfloat16)  # next input depends on this output
+    return outs
+
+
+@pytest.mark.parametrize("flags", [sk.SGEMM_FLAG_PDL,
+                                   sk.SGEMM_FLAG_PDL | sk.SGEMM_FLAG_WEIGHTS_READONLY])
+@pytest.mark.parametrize("split", [1, 3])
+def test_pdl_chain_matches_plain_launches(flags, split):
+    M = 2
+    shapes = [(4096, 4096), (4096, 4096), (2048, 4096), (4096, 2048)]
+    Ws = [synth.normal_bf16(s, synth.W_STD, seed=40 + i).to(DEV) for i, s in enumerate(shapes)]
+    xd = synth.normal_bf16((M, 4096), 1.0, seed=39).to(DEV)
+    ref = _chain(xd, Ws, 0, split)
+    torch.cuda.synchronize()
+    got = _chain(xd, Ws, flags, split)
+    torch.cuda.synchronize()
+    for a, b in zip(ref, got):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    # and under graph capture
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            gout = _chain(xd, Ws, flags, split)
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(ref, gout):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
