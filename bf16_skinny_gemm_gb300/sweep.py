@@ -1,0 +1,205 @@
+"""Offline plan sweep: time every compiled plan on each decode shape and write
+the fastest into ``csrc/plan_table.inc``.
+
+Protocol (after vLLM PR #62949, Details: "a CUDA-graph sweep over block_size,
+outputs_per_block, k_unroll, vector_width ... with the weight rotated out of
+L2", and PR #65306, Validation: a chain over copies of the weight adding up to
+at least 1 GiB, captured in a CUDA graph, trials interleaved):
+
+- for each (N, K): R weight copies with R * |W| >= max(1 GiB, 4 x L2), so every
+  GEMM of a chain reads its weights from HBM;
+- for each M and each candidate plan (every compiled kernel configuration x
+  CTA size x split factor): one CUDA graph of R GEMMs through the public
+  ``sgemm_bf16_skinny_ex`` call, launched with the decode-chain launch flags
+  (programmatic dependent launch, weights read-only);
+- T trials of P replays each, interleaved across candidates; the score is the
+  median per-GEMM time.  The fastest candidate is kept.  (The pages keep a
+  plan only if it beats cuBLAS by 5 %; here there is no other library to fall
+  back to, so the table keeps the fastest plan outright.)
+
+The batched pair shape (4096, 128) is swept as it is used: two problems per
+launch.
+
+Usage (on the GPU):
+    python -m bf16_skinny_gemm_gb300.sweep --out bf16_skinny_gemm_gb300/csrc/plan_table.inc
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import time
+
+import torch
+
+import bf16_skinny_gemm_gb300 as sk
+from bf16_skinny_gemm_gb300 import synth
+
+DECODE_SHAPES = [(12576, 4096), (4096, 4096), (2048, 4096), (4096, 1024), (8192, 1536),
+                 (4096, 8192), (77440, 4096)]
+PAIR_SHAPE = (4096, 128)
+HERE = os.path.dirname(os.path.abspath(__file__))
+DEFAULT_OUT = os.path.join(HERE, "csrc", "plan_table.inc")
+
+
+def candidates(M, N, K, splits):
+    out = []
+    for i in range(sk.sgemm_plan_count()):
+        base = sk.sgemm_plan_get(i)
+        for s in splits:
+            p = base.copy(split_k=s)
+            if sk.sgemm_plan_check(p, M, N, K) == sk.SGEMM_OK:
+                out.append(p)
+    return out
+
+
+def sweep_shape(N, K, Ms, splits, flags, trials, replays, min_bytes, pair=False, log=print):
+    dev = torch.device("cuda")
+    R = max(2, math.ceil(min_bytes / (2 * N * K)))
+    if pair:
+        R += R % 2
+    std = synth.PAIR_W_STD if pair else synth.W_STD
+    W = torch.empty((R, N, K), dtype=torch.bfloat16, device=dev)
+    for i in range(R):
+        W[i].copy_(synth.normal_bf16((N, K), std, seed=i, device=dev))
+    results = {}
+    for M in Ms:
+        x = synth.normal_bf16((R, M, K), synth.X_STD, seed=1000 + M, device=dev)
+        y = torch.empty((R, M, N), dtype=torch.bfloat16, device=dev)
+        cands = candidates(M, N, K, splits)
+        heur = sk.sgemm_plan_select(N, K, M)
+        graphs = []
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+
+        def chain(plan, fl):
+            if pair:
+                for i in range(0, R, 2):
+                    sk.sgemm_bf16_skinny_batched_ex([(x[i], W[i], y[i]), (x[i + 1], W[i + 1], y[i + 1])],
+                                                    plan=plan, flags=fl)
+            else:
+                for i in range(R):
+                    sk.sgemm_bf16_skinny_ex(x[i], W[i], y[i], plan=plan, flags=fl)
+
+        for p in cands:
+            chain(p, 0)  # eager once (split-K scratch is allocated outside capture)
+        torch.cuda.synchronize()
+        for p in cands:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    chain(p, flags)
+            graphs.append(g)
+        torch.cuda.current_stream().wait_stream(s)
+        for g in graphs:
+            g.replay()
+            g.replay()
+        torch.cuda.synchronize()
+        times = [[] for _ in cands]
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        for _ in range(trials):
+            for ci, g in enumerate(graphs):
+                e0.record()
+                for _ in range(replays):
+                    g.replay()
+                e1.record()
+                e1.synchronize()
+                per_launch = R // 2 if pair else R
+                times[ci].append(e0.elapsed_time(e1) * 1e3 / replays / per_launch)
+        med = [statistics.median(t) for t in times]
+        order = sorted(range(len(cands)), key=lambda i: med[i])
+        best = cands[order[0]]
+        nbytes = (2 if pair else 1) * 2 * (N * K + M * K + M * N)
+        heur_us = next((med[i] for i, p in enumerate(cands)
+                        if p.as_dict() == heur.as_dict()), None)
+        results[M] = {"plan": best.as_dict(), "us": med[order[0]],
+                      "gbs": nbytes / med[order[0]] / 1e3,
+                      "heuristic_us": heur_us,
+                      "top": [(cands[i].as_dict(), round(med[i], 3)) for i in order[:5]],
+                      "copies": R, "candidates": len(cands)}
+        log(f"  N={N} K={K} M={M}: best {med[order[0]]:.3f} us "
+            f"({results[M]['gbs']:.0f} GB/s) {_short(best)}; heuristic "
+            f"{heur_us if heur_us is None else round(heur_us, 3)} us; {len(cands)} candidates")
+        del graphs
+        torch.cuda.synchronize()
+    del W
+    torch.cuda.empty_cache()
+    return results
+
+
+def _short(p):
+    return (f"v{p.variant} t{p.threads} R{p.rows_per_warp} L{p.lanes_per_row} "
+            f"U{p.k_unroll} S{p.split_k}")
+
+
+def write_table(entries, path, note):
+    lines = [
+        "// Generated by bf16_skinny_gemm_gb300/sweep.py -- do not edit by hand.",
+        f"// {note}",
+        "// Fields: N, K, M, variant, threads, R, LPR, U, split, stages, ctas_per_sm",
+    ]
+    for (N, K, M), r in sorted(entries.items()):
+        p = r["plan"]
+        lines.append(
+            f"{{{N}, {K}, {M}, {p['variant']}, {p['threads']}, {p['rows_per_warp']}, "
+            f"{p['lanes_per_row']}, {p['k_unroll']}, {p['split_k']}, {p['stages']}, "
+            f"{p['ctas_per_sm']}}},  // {r['us']:.3f} us, {r['gbs']:.0f} GB/s")
+    with open(path, "w") as f:
+        f.write("\n".join(lines) + "\n")
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--out", default=DEFAULT_OUT)
+    ap.add_argument("--json", default=None, help="also write all timings here")
+    ap.add_argument("--ms", default="1,2,3,4")
+    ap.add_argument("--splits", default="1,2,4")
+    ap.add_argument("--trials", type=int, default=5)
+    ap.add_argument("--replays", type=int, default=10)
+    ap.add_argument("--min-bytes", type=float, default=float(1 << 30))
+    ap.add_argument("--shapes", default=None, help="e.g. 4096x4096,2048x4096 (default: all)")
+    ap.add_argument("--no-pair", action="store_true")
+    args = ap.parse_args(argv)
+
+    assert torch.cuda.is_available(), "the sweep runs on the GPU"
+    sk.load()
+    sk.sgemm_init()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    min_bytes = max(args.min_bytes, 4 * l2)
+    Ms = [int(v) for v in args.ms.split(",")]
+    splits = [int(v) for v in args.splits.split(",")]
+    flags = sk.SGEMM_FLAG_PDL | sk.SGEMM_FLAG_WEIGHTS_READONLY
+    shapes = DECODE_SHAPES
+    if args.shapes:
+        shapes = [tuple(int(v) for v in t.split("x")) for t in args.shapes.split(",")]
+    t0 = time.time()
+    entries, dump = {}, {}
+    for (N, K) in shapes:
+        res = sweep_shape(N, K, Ms, splits, flags, args.trials, args.replays, min_bytes)
+        for M, r in res.items():
+            entries[(N, K, M)] = r
+            dump[f"{N}x{K}x{M}"] = r
+    if not args.no_pair:
+        N, K = PAIR_SHAPE
+        res = sweep_shape(N, K, Ms, splits, flags, args.trials, args.replays, min_bytes, pair=True)
+        for M, r in res.items():
+            entries[(N, K, M)] = r
+            dump[f"{N}x{K}x{M}-pair"] = r
+    note = (f"{torch.cuda.get_device_name(0)}, {len(entries)} entries, cold L2 (>= "
+            f"{min_bytes / 2**30:.2f} GiB of weight copies per shape), launch flags PDL|readonly, "
+            f"{args.trials} interleaved trials x {args.replays} graph replays, median")
+    write_table(entries, args.out, note)
+    if args.json:
+        with open(args.json, "w") as f:
+            json.dump(dump, f, indent=1)
+    print(f"wrote {args.out} ({len(entries)} entries) in {time.time() - t0:.0f} s")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
