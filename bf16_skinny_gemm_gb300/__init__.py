@@ -26,7 +26,7 @@ __all__ = [
     "sgemm_bf16_skinny_splitk_noalloc", "NOALLOC_SCRATCH_BYTES",
     "SGEMM_OK", "SGEMM_ERR_INVALID_ARG", "SGEMM_ERR_UNSUPPORTED_SHAPE", "SGEMM_ERR_MISALIGNED",
     "SGEMM_ERR_UNSUPPORTED_DEVICE", "SGEMM_ERR_NO_WORKSPACE", "SGEMM_ERR_CUDA", "MAX_BATCH",
-    "SGEMM_VARIANT_LDG", "SGEMM_VARIANT_LDG_MIXFMA", "SGEMM_FLAG_PDL",
+    "SGEMM_VARIANT_LDG", "SGEMM_VARIANT_LDG_MIXFMA", "SGEMM_VARIANT_MMA", "SGEMM_FLAG_PDL",
     "SGEMM_FLAG_WEIGHTS_READONLY",
 ]
 
@@ -40,6 +40,7 @@ SGEMM_ERR_CUDA = 6
 MAX_BATCH = 8
 SGEMM_VARIANT_LDG = 0
 SGEMM_VARIANT_LDG_MIXFMA = 1
+SGEMM_VARIANT_MMA = 2
 SGEMM_FLAG_PDL = 1
 SGEMM_FLAG_WEIGHTS_READONLY = 2
 

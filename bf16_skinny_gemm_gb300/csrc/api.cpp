@@ -70,16 +70,11 @@ struct DeviceState {
 std::mutex g_mu;
 std::map<int, DeviceState> g_dev;
 
-// kps: K elements per split, a multiple of 8; every split non-empty.
-int split_kps(int K, int split) {
-    const int chunks = K / 8;
-    const int per = (chunks + split - 1) / split;
-    return per * 8;
-}
 
 sgemm_status_t check_plan(const sgemm_plan_t &p, int M, int N, int K) {
     (void)N;
-    if (p.variant != SGEMM_VARIANT_LDG && p.variant != SGEMM_VARIANT_LDG_MIXFMA)
+    if (p.variant != SGEMM_VARIANT_LDG && p.variant != SGEMM_VARIANT_LDG_MIXFMA &&
+        p.variant != SGEMM_VARIANT_MMA)
         return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.threads < 32 || p.threads > sk::kMaxThreads || p.threads % 32) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.vec_bytes != 16 || p.stages != 0) return SGEMM_ERR_UNSUPPORTED_SHAPE;
@@ -87,9 +82,10 @@ sgemm_status_t check_plan(const sgemm_plan_t &p, int M, int N, int K) {
     if (p.ctas_per_sm < 0 || p.ctas_per_sm > 32) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (!find_kernel(p.variant, M, p.rows_per_warp, p.lanes_per_row, p.k_unroll))
         return SGEMM_ERR_UNSUPPORTED_SHAPE;
-    const int kps = split_kps(K, p.split_k);
+    if (p.variant == SGEMM_VARIANT_MMA && p.threads < 64) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    const int kps = sk::split_kps(K, p.split_k);
     if (static_cast<long long>(p.split_k - 1) * kps >= K) return SGEMM_ERR_UNSUPPORTED_SHAPE;
-    if (static_cast<size_t>(M) * kps * 2 > kMaxSmem) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (sk::smem_bytes(p, M, kps) > kMaxSmem) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     return SGEMM_OK;
 }
 
@@ -224,8 +220,8 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
     const KernelInfo *ki = find_kernel(plan.variant, M, plan.rows_per_warp, plan.lanes_per_row,
                                        plan.k_unroll);
     const int split = plan.split_k;
-    const int kps = split_kps(K, split);
-    const size_t smem = static_cast<size_t>(M) * kps * 2;
+    const int kps = sk::split_kps(K, split);
+    const size_t smem = sk::smem_bytes(plan, M, kps);
 
     sk::Params prm;
     std::memset(&prm, 0, sizeof(prm));
@@ -240,8 +236,7 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
     prm.K = K;
     prm.kps = kps;
     prm.split = split;
-    const int rows_per_task = (32 / plan.lanes_per_row) * plan.rows_per_warp;
-    prm.row_groups = (N + rows_per_task - 1) / rows_per_task;
+    prm.row_groups = sk::work_units(plan, N);
     prm.flags = static_cast<int>(flags);
 
     int grid_x = 0;
@@ -261,8 +256,7 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
         }
         const int occ = plan.ctas_per_sm > 0 ? plan.ctas_per_sm
                                              : occupancy(*st, ki->fn, plan.threads, smem);
-        const int warps = plan.threads / 32;
-        const long long need_ctas = (prm.row_groups + warps - 1) / warps;
+        const long long need_ctas = sk::ctas_wanted(plan, N);
         const long long slots = std::max<long long>(1, static_cast<long long>(st->sms) * occ /
                                                            (static_cast<long long>(split) * batch));
         grid_x = static_cast<int>(std::max<long long>(1, std::min(need_ctas, slots)));
@@ -307,6 +301,39 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
 }
 
 }  // namespace
+
+namespace sk {
+
+int split_kps(int K, int split) {
+    const int chunks = K / 8;
+    const int per = (chunks + split - 1) / split;
+    return per * 8;
+}
+
+size_t smem_bytes(const sgemm_plan_t &plan, int M, int kps) {
+    const size_t chunks = static_cast<size_t>(kps) / 8;
+    if (plan.variant == SGEMM_VARIANT_MMA) {
+        // x rows padded by one chunk, plus two reduction buffers [NW][16][4] floats
+        return static_cast<size_t>(M) * (chunks + 1) * 16 +
+               2 * static_cast<size_t>(plan.threads / 32) * 16 * 4 * sizeof(float);
+    }
+    return static_cast<size_t>(M) * chunks * 16;
+}
+
+int work_units(const sgemm_plan_t &plan, int N) {
+    if (plan.variant == SGEMM_VARIANT_MMA) return (N + 15) / 16;
+    const int rows_per_task = (32 / plan.lanes_per_row) * plan.rows_per_warp;
+    return (N + rows_per_task - 1) / rows_per_task;
+}
+
+long long ctas_wanted(const sgemm_plan_t &plan, int N) {
+    const long long units = work_units(plan, N);
+    if (plan.variant == SGEMM_VARIANT_MMA) return units;  // one tile per CTA at most
+    const int warps = plan.threads / 32;
+    return (units + warps - 1) / warps;
+}
+
+}  // namespace sk
 
 extern "C" {
 

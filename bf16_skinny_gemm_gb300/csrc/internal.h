@@ -59,4 +59,14 @@ extern const int kKernelCountPerM;
 // Deterministic split-K reduction kernels, one per M.
 extern const void *const kReduceKernels[kMaxM + 1];
 
+// Launch geometry shared by every entry point (defined in api.cpp).
+// K elements per split: a multiple of 8, every split non-empty.
+int split_kps(int K, int split);
+// Dynamic shared memory of one CTA of this plan.
+size_t smem_bytes(const sgemm_plan_t &plan, int M, int kps);
+// Work units of this plan (row groups for the CUDA-core kernel, 16-row tiles
+// for the tensor-core kernel) and the CTAs that can use them.
+int work_units(const sgemm_plan_t &plan, int N);
+long long ctas_wanted(const sgemm_plan_t &plan, int N);
+
 }  // namespace sk

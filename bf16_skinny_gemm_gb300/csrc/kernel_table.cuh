@@ -6,6 +6,7 @@
 #pragma once
 
 #include "skinny_ldg.cuh"
+#include "skinny_mma.cuh"
 
 #define SK_LDG_CONFIGS(X, M)   \
     X(M, 1, 32, 8, false)      \
@@ -24,5 +25,15 @@
     {(MIX) ? SGEMM_VARIANT_LDG_MIXFMA : SGEMM_VARIANT_LDG, M, R, LPR, U,                 \
      reinterpret_cast<const void *>(&skinny_ldg_kernel<M, R, LPR, U, MIX>)},
 
+// Tensor-core configurations: (M, k-blocks per batch U).  R = 16 rows per tile,
+// 4 lanes share a row segment.
+#define SK_MMA_CONFIGS(X, M) \
+    X(M, 2)                  \
+    X(M, 4)                  \
+    X(M, 8)
+
+#define SK_MMA_ENTRY(M, U) \
+    {SGEMM_VARIANT_MMA, M, 16, 4, U, reinterpret_cast<const void *>(&skinny_mma_kernel<M, U>)},
+
 #define SK_DEFINE_TABLE(M, NAME) \
-    const KernelInfo NAME[] = {SK_LDG_CONFIGS(SK_LDG_ENTRY, M)};
+    const KernelInfo NAME[] = {SK_LDG_CONFIGS(SK_LDG_ENTRY, M) SK_MMA_CONFIGS(SK_MMA_ENTRY, M)};

@@ -11,9 +11,10 @@
 // instead uses the file-scope array below, which is part of the library's
 // device image and is created when the library's code is loaded on a device.
 //
-// The kernels are the regular ones (skinny_ldg_kernel with gridDim.y splits,
-// then splitk_reduce_kernel); only where the FP32 partial sums live differs,
-// so results are bitwise equal to sgemm_bf16_skinny_ex with the same plan.
+// The kernels are the regular ones of the selected plan (the streaming kernel
+// with gridDim.y splits, then splitk_reduce_kernel); only where the FP32
+// partial sums live differs, so results are bitwise equal to
+// sgemm_bf16_skinny_ex with the same plan and split.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -121,9 +122,8 @@ extern "C" sgemm_status_t sgemm_bf16_skinny_splitk_noalloc(
     s = setup_current_device(&st);
     if (s != SGEMM_OK) return s;
 
-    const int chunks = K / 8;
-    const int kps = (chunks + split_k - 1) / split_k * 8;
-    const size_t smem = static_cast<size_t>(M) * kps * 2;
+    const int kps = sk::split_kps(K, split_k);
+    const size_t smem = sk::smem_bytes(plan, M, kps);
 
     sk::Params prm = {};
     prm.item[0].x = x;
@@ -136,16 +136,14 @@ extern "C" sgemm_status_t sgemm_bf16_skinny_splitk_noalloc(
     prm.K = K;
     prm.kps = kps;
     prm.split = split_k;
-    const int rows_per_task = (32 / plan.lanes_per_row) * plan.rows_per_warp;
-    prm.row_groups = (N + rows_per_task - 1) / rows_per_task;
+    prm.row_groups = sk::work_units(plan, N);
 
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, ki->fn, plan.threads, smem) !=
             cudaSuccess ||
         occ < 1)
         occ = 1;
-    const int warps = plan.threads / 32;
-    const long long need = (prm.row_groups + warps - 1) / warps;
+    const long long need = sk::ctas_wanted(plan, N);
     long long slots = static_cast<long long>(st->sms) * occ / split_k;
     if (slots < 1) slots = 1;
     const int grid_x = static_cast<int>(need < slots ? need : slots);

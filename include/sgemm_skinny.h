@@ -89,8 +89,13 @@ enum {
     SGEMM_VARIANT_LDG = 0,        /* W streamed with 128-bit non-allocating loads into a ring of
                                      registers, x staged in shared memory, BF16 widened to FP32,
                                      FP32 FMA, warp-shuffle reduction */
-    SGEMM_VARIANT_LDG_MIXFMA = 1  /* the same with the mixed-precision FMA (BF16 operands, FP32
+    SGEMM_VARIANT_LDG_MIXFMA = 1, /* the same with the mixed-precision FMA (BF16 operands, FP32
                                      addend): fewer instructions, bitwise-identical results */
+    SGEMM_VARIANT_MMA = 2         /* W streamed the same way into mma.sync m16n8k16 tensor-core
+                                     fragments (x padded to 8 columns); a CTA of NW warps splits
+                                     each 16-row tile's K range and adds the NW partial tiles in
+                                     shared memory.  rows_per_warp = 16, lanes_per_row = 4,
+                                     k_unroll = 32-element k-blocks per batch */
 };
 
 /* Launch flags (bit set) for the _ex calls.

@@ -325,9 +325,10 @@ def test_batched_graph_replay():
 # ------------------------------------------- plan equivalence and launch flags
 @pytest.mark.parametrize("M", [1, 3, 4])
 def test_plans_with_same_lanes_per_row_agree_bitwise(M):
-    """The accumulation order depends only on (K range, lanes per row): the
-    mixed-precision FMA and the widened FP32 FMA, any R, U and CTA size must
-    give the same bits."""
+    """For the CUDA-core kernels the accumulation order depends only on (K range,
+    lanes per row): the mixed-precision FMA and the widened FP32 FMA, any R, U
+    and CTA size must give the same bits.  For the tensor-core kernel it
+    depends on (K range, warps per CTA): any U must give the same bits."""
     N, K = 1500, 3072
     x, W = _inputs(M, N, K, seed=31)
     xd, Wd = x.to(DEV), W.to(DEV)
@@ -337,13 +338,14 @@ def test_plans_with_same_lanes_per_row_agree_bitwise(M):
             plan = p.copy(split_k=split)
             y = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=plan)
             torch.cuda.synchronize()
-            key = (plan.lanes_per_row, split)
+            mma = plan.variant == sk.SGEMM_VARIANT_MMA
+            key = (mma, plan.lanes_per_row, split, plan.threads if mma else 0)
             if key in by_lpr:
                 assert torch.equal(by_lpr[key][1].view(torch.int16), y.view(torch.int16)), \
                     (by_lpr[key][0], plan)
             else:
                 by_lpr[key] = (plan, y)
-    for (lpr, split), (plan, y) in by_lpr.items():
+    for _, (plan, y) in by_lpr.items():
         _check(x, W, y)
 
 
