@@ -108,14 +108,19 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# The streaming kernels' sources, their compiled configurations, the plan table and
+# the launch geometry: what the recorded DRAM traffic per launch depends on.
+KERNEL_SOURCES = ["skinny_ldg.cuh", "skinny_mma.cuh", "kernel_table.cuh", "internal.h",
+                  "plan_table.inc", "api.cpp"]
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bf16_skinny_gemm_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")) and not name.startswith("."):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -393,6 +398,178 @@ def reference_arm(args):
     return 0
 
 
+def _time_graphs(torch, dist, graphs, steps, warmup):
+    """Replay each graph `warmup` then `steps` times; per-graph median ms and the
+    max-over-ranks total seconds of the timed replays."""
+    for _ in range(warmup):
+        for g in graphs:
+            g.replay()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
+          for _ in range(steps)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(steps):
+        ev[i][0].record()
+        for j, g in enumerate(graphs):
+            g.replay()
+            ev[i][j + 1].record()
+    stop.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    per = [statistics.median(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps))
+           for j in range(len(graphs))]
+    return per, dist.max(start.elapsed_time(stop) / 1e3)
+
+
+def _capture(torch, fn):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return g
+
+
+def run_pairs(args, torch, sk, synth, dist, min_bytes):
+    """Paired projection f_b / g_b, (N, K) = (4096, 128), M = 1..4: both problems
+    in ONE batched launch, against two separate launches of the same kernel
+    (vLLM PR #57617, Microbenchmark table: two Linear calls vs one paired call).
+    Weights rotate through copies totalling >= 4 x L2 (cold)."""
+    ws, rank, _ = dist_info()
+    N, K = PAIR
+    dev = torch.device("cuda")
+    R = max(2, math.ceil(min_bytes / (2 * 2 * N * K)))
+    W = torch.empty((R, 2, N, K), dtype=torch.bfloat16, device=dev)
+    for i in range(R):
+        for j in range(2):
+            W[i, j].copy_(synth.normal_bf16((N, K), synth.PAIR_W_STD, seed=2 * i + j, device=dev))
+    flags = sk.SGEMM_FLAG_PDL | sk.SGEMM_FLAG_WEIGHTS_READONLY
+    # every buffer a captured graph uses must outlive the graph: entering a graph
+    # capture empties the allocator cache, so a freed buffer would be unmapped
+    detail, graphs, nbytes, keep = [], [], 0, []
+    for M in SWEEP_MS + [3]:
+        x = synth.normal_bf16((R, 2, M, K), synth.X_STD, seed=100 + M, device=dev)
+        y = torch.empty((R, 2, M, N), dtype=torch.bfloat16, device=dev)
+        keep.append((x, y))
+
+        def paired():
+            for i in range(R):
+                sk.sgemm_bf16_skinny_batched_ex([(x[i, 0], W[i, 0], y[i, 0]),
+                                                 (x[i, 1], W[i, 1], y[i, 1])], flags=flags)
+
+        def separate():
+            for i in range(R):
+                for j in range(2):
+                    sk.sgemm_bf16_skinny_ex(x[i, j], W[i, j], y[i, j], flags=flags)
+
+        paired()
+        separate()
+        torch.cuda.synchronize()
+        graphs += [_capture(torch, paired), _capture(torch, separate)]
+        detail.append({"M": M, "copies": R})
+        nbytes += R * 2 * gemm_bytes(M, N, K)
+    per, _ = _time_graphs(torch, dist, graphs, args.steps, args.warmup)
+    del graphs, keep
+    total_ms = 0.0
+    for d, (p_ms, s_ms) in zip(detail, zip(per[0::2], per[1::2])):
+        d["us_per_paired_launch"] = round(p_ms * 1e3 / d["copies"], 3)
+        d["us_two_launches"] = round(s_ms * 1e3 / d["copies"], 3)
+        b = 2 * gemm_bytes(d["M"], N, K)
+        d["gbs_paired"] = round(b / (p_ms * 1e3 / d["copies"]) / 1e3, 1)
+        total_ms += p_ms
+    value = dist.sum(nbytes) / (dist.max(total_ms) / 1e3) / 1e9
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "paired batched projection f_b/g_b: batch 2 x (N,K)=(4096,128), "
+                                   "M=1..4, one launch for both",
+                       "x": "BF16 ~ N(0,1)", "W": "BF16 ~ N(0,0.05^2)",
+                       "l2": "inputs larger than L2 (rotating weight copies)",
+                       "launch_flags": "pdl,readonly", "parallelism": "replicas"},
+            "gpu_launches": sum(d["copies"] * 3 for d in detail) * args.steps,
+            "detail": detail}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+        if args.detail_out:
+            with open(args.detail_out, "w") as f:
+                json.dump(line, f, indent=1)
+    dist.close()
+    return 0
+
+
+def run_chain(args, torch, sk, synth, dist):
+    """Decode-step chain at M=1: 186 GEMMs on distinct weights in the order
+    (12576,4096)x34, (4096,4096)x34, (2048,4096)x53, (4096,1024)x42,
+    (8192,1536)x11, (4096,8192)x11, (77440,4096)x1 (7.5 GB of weights, so every
+    GEMM is cold), each output fed through the elementwise rescale kernel into
+    the next GEMM's input, the whole step one CUDA graph.  The elementwise
+    kernels are also timed alone and subtracted (as vLLM PR #65306 does)."""
+    ws, rank, _ = dist_info()
+    dev = torch.device("cuda")
+    seq = [shape for shape, count in CHAIN for _ in range(count)]
+    Ws = [synth.normal_bf16(shape, synth.W_STD, seed=i, device=dev) for i, shape in enumerate(seq)]
+    xs = [torch.empty((1, K), dtype=torch.bfloat16, device=dev) for (_, K) in seq]
+    ys = [torch.empty((1, N), dtype=torch.bfloat16, device=dev) for (N, _) in seq]
+    xs[0].copy_(synth.normal_bf16((1, seq[0][1]), synth.X_STD, seed=999, device=dev))
+    scales = [1.0 / (synth.W_STD * math.sqrt(K)) for (_, K) in seq]
+    flags = sk.SGEMM_FLAG_PDL | sk.SGEMM_FLAG_WEIGHTS_READONLY
+    if args.flags == "none":
+        flags = 0
+
+    def step():
+        for i in range(len(seq)):
+            sk.sgemm_bf16_skinny_ex(xs[i], Ws[i], ys[i], flags=flags)
+            if i + 1 < len(seq):
+                sk.sgemm_bf16_rescale(ys[i], xs[i + 1], scales[i], flags=flags & sk.SGEMM_FLAG_PDL)
+
+    def elementwise_only():
+        for i in range(len(seq) - 1):
+            sk.sgemm_bf16_rescale(ys[i], xs[i + 1], scales[i], flags=flags & sk.SGEMM_FLAG_PDL)
+
+    step()
+    torch.cuda.synchronize()
+    g_step = _capture(torch, step)
+    g_elt = _capture(torch, elementwise_only)
+    per, total_s = _time_graphs(torch, dist, [g_step, g_elt], args.steps, args.warmup)
+    step_ms, elt_ms = per
+    w_bytes = sum(2 * N * K for (N, K) in seq)
+    alg = sum(gemm_bytes(1, N, K) for (N, K) in seq)
+    gemm_ms = step_ms - elt_ms
+    peak, src = measured_peaks()
+    value = dist.sum(alg) / (dist.max(gemm_ms) / 1e3) / 1e9
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "decode-step chain at M=1, 186 GEMMs on distinct weights, "
+                                   "elementwise rescale between GEMMs, one CUDA graph",
+                       "weights_bytes": w_bytes, "l2": "inputs larger than L2 (7.5 GB of "
+                       "distinct weights per step)", "launch_flags": args.flags,
+                       "parallelism": "replicas"},
+            "chain": {"step_us": round(step_ms * 1e3, 1),
+                      "elementwise_us": round(elt_ms * 1e3, 1),
+                      "gemm_us": round(gemm_ms * 1e3, 1),
+                      "gemm_us_at_measured_peak": round(alg / (peak * 1e9) * 1e6, 1),
+                      "frac_of_peak": round(alg / (gemm_ms / 1e3) / 1e9 / peak, 4),
+                      "peak_source": src},
+            "gpu_launches": (2 * len(seq) - 1) * args.steps}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+        if args.detail_out:
+            with open(args.detail_out, "w") as f:
+                json.dump(line, f, indent=1)
+    dist.close()
+    return 0
+
+
 def sweep_config_desc(gs):
     d = {"workload": "shape sweep at M=1,2,4 over local (N,K) = " +
                      ", ".join(f"({N},{K})" for N, K in SWEEP_SHAPES),
@@ -463,8 +640,10 @@ def main():
         cases = [(4096, 1024, 1)]
     elif args.workload == "lmhead":
         cases = [(LMHEAD[0], LMHEAD[1], M) for M in SWEEP_MS]
+    elif args.workload == "pairs":
+        return run_pairs(args, torch, sk, synth, dist, min_bytes)
     else:
-        raise SystemExit(f"workload {args.workload!r} is not available yet")
+        return run_chain(args, torch, sk, synth, dist)
 
     flags = 0
     for f in args.flags.split(","):
@@ -506,8 +685,8 @@ def main():
         kern_bytes += c["R"] * b * len(ms)
         kern_ms += sum(ms)
         key = (c["N"], c["K"], c["M"])
-        if key in traffic:
-            traffic_sum += traffic[key]
+        if key in traffic:  # weighted like the achieved bytes: by launches in the step
+            traffic_sum += traffic[key] * c["R"]
             traffic_cnt += 1
     for d in detail:
         base = [e for e in detail if e["N"] == d["N"] and e["K"] == d["K"] and e["M"] == 1]
@@ -518,9 +697,10 @@ def main():
     launches_timed = sum(c["R"] for c in gs.cases) * args.steps
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (copy bandwidth)",
-                "traffic": (round(traffic_sum / traffic_cnt) if traffic_cnt == len(gs.cases)
-                            else None),
-                "traffic_note": ("mean DRAM bytes per launch over the (N,K,M) cases, from ncu"
+                "traffic": (round(traffic_sum / sum(c["R"] for c in gs.cases))
+                            if traffic_cnt == len(gs.cases) else None),
+                "traffic_note": ("DRAM bytes per launch of the step (ncu, per case, weighted by "
+                                 "launches like 'achieved')"
                                  if traffic_cnt == len(gs.cases) else traffic_src),
                 "algorithmic_bytes_per_launch": round(kern_bytes / launches_timed)}
 

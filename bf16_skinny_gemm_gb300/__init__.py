@@ -23,7 +23,7 @@ __all__ = [
     "sgemm_bf16_skinny", "sgemm_bf16_skinny_ex", "sgemm_bf16_skinny_batched",
     "sgemm_bf16_skinny_batched_ex", "sgemm_plan_select", "sgemm_plan_count", "sgemm_plan_get",
     "sgemm_plan_check", "sgemm_init", "sgemm_status_string", "sgemm_version",
-    "sgemm_bf16_skinny_splitk_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "sgemm_bf16_skinny_splitk_noalloc", "NOALLOC_SCRATCH_BYTES", "sgemm_bf16_rescale",
     "SGEMM_OK", "SGEMM_ERR_INVALID_ARG", "SGEMM_ERR_UNSUPPORTED_SHAPE", "SGEMM_ERR_MISALIGNED",
     "SGEMM_ERR_UNSUPPORTED_DEVICE", "SGEMM_ERR_NO_WORKSPACE", "SGEMM_ERR_CUDA", "MAX_BATCH",
     "SGEMM_VARIANT_LDG", "SGEMM_VARIANT_LDG_MIXFMA", "SGEMM_VARIANT_MMA", "SGEMM_FLAG_PDL",
@@ -123,6 +123,8 @@ def load() -> ctypes.CDLL:
         lib.sgemm_status_string.restype = ctypes.c_char_p
         lib.sgemm_bf16_skinny_splitk_noalloc.argtypes = [vp, ll, vp, vp, ll, ci, ci, ci, ci, vp]
         lib.sgemm_bf16_skinny_splitk_noalloc.restype = ci
+        lib.sgemm_bf16_rescale.argtypes = [vp, ll, vp, ll, ctypes.c_float, cu, vp]
+        lib.sgemm_bf16_rescale.restype = ci
         lib.sgemm_version.argtypes = []
         lib.sgemm_version.restype = ctypes.c_char_p
         _lib = lib
@@ -230,6 +232,19 @@ def sgemm_bf16_skinny_batched_ex(items, plan: Plan | None = None, flags: int = 0
                                                int(flags), _stream(stream)),
            "sgemm_bf16_skinny_batched_ex")
     return outs
+
+
+def sgemm_bf16_rescale(y: torch.Tensor, x: torch.Tensor, scale: float, flags: int = 0,
+                       stream=None) -> torch.Tensor:
+    """``x.view(-1)[k] = bf16(float(y.view(-1)[k % y.numel()]) * scale)`` on the GPU: the
+    elementwise step between two GEMMs of a decode chain.  Returns x."""
+    for t, name in ((y, "y"), (x, "x")):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+    _check(load().sgemm_bf16_rescale(y.data_ptr(), y.numel(), x.data_ptr(), x.numel(),
+                                     float(scale), int(flags), _stream(stream)),
+           "sgemm_bf16_rescale")
+    return x
 
 
 NOALLOC_SCRATCH_BYTES = 4 << 20

@@ -182,6 +182,16 @@ sgemm_status_t sgemm_plan_check(const sgemm_plan_t *plan, int M, int N, int K);
  * streams must be ordered by the caller. */
 sgemm_status_t sgemm_init(void);
 
+/* The elementwise step between consecutive GEMMs of a decode chain ("a small
+ * kernel between GEMMs", vLLM PR #65306, Validation):
+ *     x[k] = RNE_bf16( float(y[k mod n_src]) * scale )   for 0 <= k < n_dst.
+ * y and x are DEVICE arrays of BF16 bits (2-byte aligned, not overlapping).
+ * flags: SGEMM_FLAG_PDL launches it as a programmatic dependent (it waits for
+ * the previous kernel before reading y).  Errors as for the GEMM calls. */
+sgemm_status_t sgemm_bf16_rescale(const sgemm_bf16_t *y, long long n_src, sgemm_bf16_t *x,
+                                  long long n_dst, float scale, unsigned flags,
+                                  sgemm_stream_t stream);
+
 /* Size of the fixed device array used by sgemm_bf16_skinny_splitk_noalloc. */
 #define SGEMM_NOALLOC_SCRATCH_BYTES (4u << 20)
 
