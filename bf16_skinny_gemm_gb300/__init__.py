@@ -26,7 +26,8 @@ __all__ = [
     "sgemm_bf16_skinny_splitk_noalloc", "NOALLOC_SCRATCH_BYTES", "sgemm_bf16_rescale",
     "SGEMM_OK", "SGEMM_ERR_INVALID_ARG", "SGEMM_ERR_UNSUPPORTED_SHAPE", "SGEMM_ERR_MISALIGNED",
     "SGEMM_ERR_UNSUPPORTED_DEVICE", "SGEMM_ERR_NO_WORKSPACE", "SGEMM_ERR_CUDA", "MAX_BATCH",
-    "SGEMM_VARIANT_LDG", "SGEMM_VARIANT_LDG_MIXFMA", "SGEMM_VARIANT_MMA", "SGEMM_FLAG_PDL",
+    "SGEMM_VARIANT_LDG", "SGEMM_VARIANT_LDG_MIXFMA", "SGEMM_VARIANT_MMA", "SGEMM_VARIANT_MMA_T", "SGEMM_VARIANT_BULK", "SGEMM_FLAG_PDL",
+    "SGEMM_FLAG_TEST_STALL", "sgemm_device_errors",
     "SGEMM_FLAG_WEIGHTS_READONLY",
 ]
 
@@ -41,6 +42,9 @@ MAX_BATCH = 8
 SGEMM_VARIANT_LDG = 0
 SGEMM_VARIANT_LDG_MIXFMA = 1
 SGEMM_VARIANT_MMA = 2
+SGEMM_VARIANT_MMA_T = 3
+SGEMM_VARIANT_BULK = 4
+SGEMM_FLAG_TEST_STALL = 4
 SGEMM_FLAG_PDL = 1
 SGEMM_FLAG_WEIGHTS_READONLY = 2
 
@@ -125,6 +129,8 @@ def load() -> ctypes.CDLL:
         lib.sgemm_bf16_skinny_splitk_noalloc.restype = ci
         lib.sgemm_bf16_rescale.argtypes = [vp, ll, vp, ll, ctypes.c_float, cu, vp]
         lib.sgemm_bf16_rescale.restype = ci
+        lib.sgemm_device_errors.argtypes = [ctypes.POINTER(ctypes.c_int)]
+        lib.sgemm_device_errors.restype = ci
         lib.sgemm_version.argtypes = []
         lib.sgemm_version.restype = ctypes.c_char_p
         _lib = lib
@@ -302,6 +308,14 @@ def sgemm_plan_check(plan: Plan, M: int, N: int, K: int) -> int:
 def sgemm_init() -> None:
     """Allocate the split-K scratch of the current device (before graph capture)."""
     _check(load().sgemm_init(), "sgemm_init")
+
+
+def sgemm_device_errors() -> int:
+    """Read and clear the device error word of the current device (synchronous).
+    Bit 0: a bulk-copy kernel gave up waiting for its data and wrote NaN."""
+    v = ctypes.c_int(0)
+    _check(load().sgemm_device_errors(ctypes.byref(v)), "sgemm_device_errors")
+    return v.value
 
 
 def sgemm_status_string(status: int) -> str:

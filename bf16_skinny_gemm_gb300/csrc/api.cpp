@@ -36,7 +36,7 @@ const int kTableSize = static_cast<int>(sizeof(kTable) / sizeof(kTable[0])) - 1;
 
 constexpr int kThreadChoices[] = {256, 128};
 constexpr int kNumThreadChoices = 2;
-constexpr size_t kMaxSmem = 227 * 1024;
+constexpr size_t kMaxSmem = sk::kMaxSmemOptin;
 constexpr size_t kDefaultWorkspace = 16u << 20;
 
 const KernelInfo *table_for_m(int M) {
@@ -49,11 +49,20 @@ const KernelInfo *table_for_m(int M) {
     }
 }
 
-const KernelInfo *find_kernel(int variant, int M, int R, int LPR, int U) {
+// stages 0 is accepted as 1 (single batch in flight).
+const KernelInfo *find_kernel(int variant, int M, int R, int LPR, int U, int stages) {
     const KernelInfo *t = table_for_m(M);
     if (!t) return nullptr;
+    if (variant == SGEMM_VARIANT_BULK) {  // one kernel per M; the rest are launch parameters
+        for (int i = 0; i < sk::kKernelCountPerM; ++i)
+            if (t[i].variant == variant && t[i].R == R && t[i].LPR == LPR) return &t[i];
+        return nullptr;
+    }
+    if (stages == 0) stages = 1;
     for (int i = 0; i < sk::kKernelCountPerM; ++i)
-        if (t[i].variant == variant && t[i].R == R && t[i].LPR == LPR && t[i].U == U) return &t[i];
+        if (t[i].variant == variant && t[i].R == R && t[i].LPR == LPR && t[i].U == U &&
+            t[i].stages == stages)
+            return &t[i];
     return nullptr;
 }
 
@@ -71,18 +80,34 @@ std::mutex g_mu;
 std::map<int, DeviceState> g_dev;
 
 
+sgemm_status_t check_bulk_plan(const sgemm_plan_t &p, int M, int K) {
+    const int nw = p.threads / 32 - 1;
+    if (p.threads % 32 || nw < 2 || p.threads > sk::kMaxThreadsBulk) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (p.rows_per_warp != 8 || p.lanes_per_row != 4 || p.vec_bytes != 16)
+        return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (p.k_unroll < 1 || p.k_unroll > 128 || p.stages < 2 || p.stages > sk::kMaxRing)
+        return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (p.split_k != 1 || p.ctas_per_sm < 0 || p.ctas_per_sm > 2) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (!find_kernel(p.variant, M, 8, 4, 0, 0)) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    // leave 1 KiB for the kernel's static shared memory
+    if (sk::smem_bytes(p, M, K) + 1024 > kMaxSmem) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    return SGEMM_OK;
+}
+
 sgemm_status_t check_plan(const sgemm_plan_t &p, int M, int N, int K) {
     (void)N;
+    if (p.variant == SGEMM_VARIANT_BULK) return check_bulk_plan(p, M, K);
     if (p.variant != SGEMM_VARIANT_LDG && p.variant != SGEMM_VARIANT_LDG_MIXFMA &&
-        p.variant != SGEMM_VARIANT_MMA)
+        p.variant != SGEMM_VARIANT_MMA && p.variant != SGEMM_VARIANT_MMA_T)
         return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.threads < 32 || p.threads > sk::kMaxThreads || p.threads % 32) return SGEMM_ERR_UNSUPPORTED_SHAPE;
-    if (p.vec_bytes != 16 || p.stages != 0) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (p.vec_bytes != 16 || p.stages < 0 || p.stages > 2) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.split_k < 1 || p.split_k > 64) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.ctas_per_sm < 0 || p.ctas_per_sm > 32) return SGEMM_ERR_UNSUPPORTED_SHAPE;
-    if (!find_kernel(p.variant, M, p.rows_per_warp, p.lanes_per_row, p.k_unroll))
+    if (!find_kernel(p.variant, M, p.rows_per_warp, p.lanes_per_row, p.k_unroll, p.stages))
         return SGEMM_ERR_UNSUPPORTED_SHAPE;
-    if (p.variant == SGEMM_VARIANT_MMA && p.threads < 64) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if ((p.variant == SGEMM_VARIANT_MMA || p.variant == SGEMM_VARIANT_MMA_T) && p.threads < 64)
+        return SGEMM_ERR_UNSUPPORTED_SHAPE;
     const int kps = sk::split_kps(K, p.split_k);
     if (static_cast<long long>(p.split_k - 1) * kps >= K) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (sk::smem_bytes(p, M, kps) > kMaxSmem) return SGEMM_ERR_UNSUPPORTED_SHAPE;
@@ -122,7 +147,7 @@ sgemm_plan_t heuristic_plan(int N, int K, int M) {
         split = static_cast<int>((xbytes + budget - 1) / budget);
         split = std::max(1, std::min(split, 64));
     }
-    return make_plan(SGEMM_VARIANT_LDG_MIXFMA, 256, R, LPR, U, split, 0, 0, -1);
+    return make_plan(SGEMM_VARIANT_LDG_MIXFMA, 256, R, LPR, U, split, 1, 0, -1);
 }
 
 sgemm_status_t probe_device(int *dev_out, DeviceState **st_out) {
@@ -146,8 +171,12 @@ sgemm_status_t probe_device(int *dev_out, DeviceState **st_out) {
     return SGEMM_OK;
 }
 
-// Requires g_mu held.
+// The last kErrBytes of the scratch hold the device error word of the bulk kernel.
+constexpr size_t kErrBytes = 256;
+
+// Requires g_mu held.  `bytes` is the partial-sum space needed before the error word.
 sgemm_status_t ensure_workspace(DeviceState &st, size_t bytes, cudaStream_t stream) {
+    bytes += kErrBytes;
     if (st.ws && st.ws_bytes >= bytes) return SGEMM_OK;
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return SGEMM_ERR_NO_WORKSPACE;
@@ -162,9 +191,17 @@ sgemm_status_t ensure_workspace(DeviceState &st, size_t bytes, cudaStream_t stre
     }
     void *p = nullptr;
     if (cudaMalloc(&p, want) != cudaSuccess) return SGEMM_ERR_CUDA;
+    if (cudaMemset(static_cast<char *>(p) + want - kErrBytes, 0, kErrBytes) != cudaSuccess) {
+        cudaFree(p);
+        return SGEMM_ERR_CUDA;
+    }
     st.ws = static_cast<float *>(p);
     st.ws_bytes = want;
     return SGEMM_OK;
+}
+
+int *error_word(DeviceState &st) {
+    return reinterpret_cast<int *>(reinterpret_cast<char *>(st.ws) + st.ws_bytes - kErrBytes);
 }
 
 // Requires g_mu held.
@@ -202,7 +239,8 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
                    const sgemm_plan_t *plan_in, unsigned flags, cudaStream_t stream) {
     sgemm_status_t s = validate_common(M, N, K, batch);
     if (s != SGEMM_OK) return s;
-    if (flags & ~(SGEMM_FLAG_PDL | SGEMM_FLAG_WEIGHTS_READONLY)) return SGEMM_ERR_INVALID_ARG;
+    if (flags & ~(SGEMM_FLAG_PDL | SGEMM_FLAG_WEIGHTS_READONLY | SGEMM_FLAG_TEST_STALL))
+        return SGEMM_ERR_INVALID_ARG;
     if (!items) return SGEMM_ERR_INVALID_ARG;
     for (int b = 0; b < batch; ++b) {
         s = validate_item(items[b], N, K);
@@ -218,10 +256,11 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
     if (s != SGEMM_OK) return s;
 
     const KernelInfo *ki = find_kernel(plan.variant, M, plan.rows_per_warp, plan.lanes_per_row,
-                                       plan.k_unroll);
+                                       plan.k_unroll, plan.stages);
+    const bool bulk = plan.variant == SGEMM_VARIANT_BULK;
     const int split = plan.split_k;
-    const int kps = sk::split_kps(K, split);
-    const size_t smem = sk::smem_bytes(plan, M, kps);
+    const int kps = bulk ? 32 * plan.k_unroll : sk::split_kps(K, split);
+    const size_t smem = sk::smem_bytes(plan, M, bulk ? K : kps);
 
     sk::Params prm;
     std::memset(&prm, 0, sizeof(prm));
@@ -238,6 +277,7 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
     prm.split = split;
     prm.row_groups = sk::work_units(plan, N);
     prm.flags = static_cast<int>(flags);
+    prm.ring = bulk ? plan.stages : 0;
 
     int grid_x = 0;
     {
@@ -248,17 +288,22 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
             if (s != SGEMM_OK) return s;
             prm.ws = st->ws;
         }
+        if (bulk) {
+            s = ensure_workspace(*st, 0, stream);
+            if (s != SGEMM_OK) return s;
+            prm.err = error_word(*st);
+        }
         if (!st->smem_attr_set[ki->fn]) {
-            if (cudaFuncSetAttribute(ki->fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(kMaxSmem)) != cudaSuccess)
-                return SGEMM_ERR_CUDA;
+            if (sk::allow_max_dynamic_smem(ki->fn) != cudaSuccess) return SGEMM_ERR_CUDA;
             st->smem_attr_set[ki->fn] = true;
         }
-        const int occ = plan.ctas_per_sm > 0 ? plan.ctas_per_sm
-                                             : occupancy(*st, ki->fn, plan.threads, smem);
+        const int occ = (plan.ctas_per_sm > 0 && !bulk)
+                            ? plan.ctas_per_sm
+                            : occupancy(*st, ki->fn, plan.threads, smem);
         const long long need_ctas = sk::ctas_wanted(plan, N);
-        const long long slots = std::max<long long>(1, static_cast<long long>(st->sms) * occ /
-                                                           (static_cast<long long>(split) * batch));
+        const int occ_eff = bulk ? std::min(occ, std::max(plan.ctas_per_sm, 1)) : occ;
+        const long long slots = std::max<long long>(
+            1, static_cast<long long>(st->sms) * occ_eff / (static_cast<long long>(split) * batch));
         grid_x = static_cast<int>(std::max<long long>(1, std::min(need_ctas, slots)));
     }
 
@@ -311,24 +356,46 @@ int split_kps(int K, int split) {
 }
 
 size_t smem_bytes(const sgemm_plan_t &plan, int M, int kps) {
+    if (plan.variant == SGEMM_VARIANT_BULK) {
+        // kps is the whole K here: the bulk kernel keeps all of x in shared memory
+        const BulkLayout L(M, kps, 32 * plan.k_unroll, plan.stages, plan.threads / 32 - 1);
+        return static_cast<size_t>(L.total);
+    }
     const size_t chunks = static_cast<size_t>(kps) / 8;
     if (plan.variant == SGEMM_VARIANT_MMA) {
         // x rows padded by one chunk, plus two reduction buffers [NW][16][4] floats
         return static_cast<size_t>(M) * (chunks + 1) * 16 +
                2 * static_cast<size_t>(plan.threads / 32) * 16 * 4 * sizeof(float);
     }
+    if (plan.variant == SGEMM_VARIANT_MMA_T) {
+        // x rows padded by one chunk, plus two reduction buffers [NW][8][M] floats
+        return static_cast<size_t>(M) * (chunks + 1) * 16 +
+               2 * static_cast<size_t>(plan.threads / 32) * 8 * M * sizeof(float);
+    }
     return static_cast<size_t>(M) * chunks * 16;
 }
 
 int work_units(const sgemm_plan_t &plan, int N) {
     if (plan.variant == SGEMM_VARIANT_MMA) return (N + 15) / 16;
+    if (plan.variant == SGEMM_VARIANT_MMA_T || plan.variant == SGEMM_VARIANT_BULK)
+        return (N + 7) / 8;
     const int rows_per_task = (32 / plan.lanes_per_row) * plan.rows_per_warp;
     return (N + rows_per_task - 1) / rows_per_task;
 }
 
+cudaError_t allow_max_dynamic_smem(const void *fn) {
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, fn);
+    if (e != cudaSuccess) return e;
+    const int dyn = static_cast<int>(kMaxSmemOptin) - static_cast<int>(a.sharedSizeBytes);
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+}
+
 long long ctas_wanted(const sgemm_plan_t &plan, int N) {
     const long long units = work_units(plan, N);
-    if (plan.variant == SGEMM_VARIANT_MMA) return units;  // one tile per CTA at most
+    if (plan.variant == SGEMM_VARIANT_MMA || plan.variant == SGEMM_VARIANT_MMA_T ||
+        plan.variant == SGEMM_VARIANT_BULK)
+        return units;  // one tile per CTA at most
     const int warps = plan.threads / 32;
     return (units + warps - 1) / warps;
 }
@@ -354,8 +421,14 @@ int sgemm_plan_count(void) { return sk::kKernelCountPerM * kNumThreadChoices; }
 sgemm_status_t sgemm_plan_get(int index, sgemm_plan_t *plan) {
     if (!plan || index < 0 || index >= sgemm_plan_count()) return SGEMM_ERR_INVALID_ARG;
     const KernelInfo &k = sk::kKernelsM1[index / kNumThreadChoices];
-    *plan = make_plan(k.variant, kThreadChoices[index % kNumThreadChoices], k.R, k.LPR, k.U, 1, 0,
-                      0, -1);
+    if (k.variant == SGEMM_VARIANT_BULK) {
+        // producer warp + 8 or 4 consumer warps; 1024-wide stages, 4 ring slots
+        const int threads = (index % kNumThreadChoices) == 0 ? 288 : 160;
+        *plan = make_plan(k.variant, threads, 8, 4, 32, 1, 4, 0, -1);
+        return SGEMM_OK;
+    }
+    *plan = make_plan(k.variant, kThreadChoices[index % kNumThreadChoices], k.R, k.LPR, k.U, 1,
+                      k.stages, 0, -1);
     return SGEMM_OK;
 }
 
@@ -402,6 +475,23 @@ sgemm_status_t sgemm_init(void) {
     if (s != SGEMM_OK) return s;
     std::lock_guard<std::mutex> lk(g_mu);
     return ensure_workspace(*st, kDefaultWorkspace, nullptr);
+}
+
+sgemm_status_t sgemm_device_errors(int *flags) {
+    if (!flags) return SGEMM_ERR_INVALID_ARG;
+    *flags = 0;
+    int dev = 0;
+    DeviceState *st = nullptr;
+    sgemm_status_t s = probe_device(&dev, &st);
+    if (s != SGEMM_OK) return s;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!st->ws) return SGEMM_OK;
+    if (cudaDeviceSynchronize() != cudaSuccess) return SGEMM_ERR_CUDA;
+    int *w = error_word(*st);
+    if (cudaMemcpy(flags, w, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(w, 0, sizeof(int)) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
+    return SGEMM_OK;
 }
 
 const char *sgemm_status_string(sgemm_status_t status) {

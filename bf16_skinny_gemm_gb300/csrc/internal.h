@@ -13,6 +13,9 @@ namespace sk {
 constexpr int kMaxBatch = SGEMM_MAX_BATCH;
 constexpr int kMaxM = 4;
 constexpr int kMaxThreads = 256;
+constexpr int kMaxThreadsBulk = 288;  // producer warp + up to 8 consumer warps
+constexpr int kMaxRing = 16;          // ring slots of the bulk-copy kernel
+constexpr size_t kMaxSmemOptin = 227 * 1024;  // shared memory a CTA may opt in to
 
 // One problem of a (possibly batched) launch.  Row strides in elements.
 struct Item {
@@ -26,6 +29,7 @@ struct Item {
 // Params::flags bits (the launch flags of the C ABI, SGEMM_FLAG_*).
 constexpr int kFlagPdl = SGEMM_FLAG_PDL;
 constexpr int kFlagWeightsReadOnly = SGEMM_FLAG_WEIGHTS_READONLY;
+constexpr int kFlagTestStall = SGEMM_FLAG_TEST_STALL;
 
 // Kernel parameters (passed by value; about 350 bytes).
 struct Params {
@@ -37,6 +41,33 @@ struct Params {
     int split;       // number of K splits (gridDim.y)
     int row_groups;  // ceil(N / rows per warp task)
     int flags;       // SGEMM_FLAG_* bits
+    int ring;        // bulk-copy kernel: shared-memory ring slots
+    int *err;        // bulk-copy kernel: device error word (bit 0: a wait gave up); may be null
+};
+
+#ifdef __CUDACC__
+#define SK_HD __host__ __device__
+#else
+#define SK_HD
+#endif
+
+// Shared-memory layout of one CTA (all offsets 16-byte aligned):
+//   [0, 256)          mbarriers: full[S], empty[S]  (S <= 16)
+//   x                 M rows of K BF16, row stride K*2 + 16 bytes
+//   ring              S slots of 8 rows x KS BF16, row stride KS*2 + 16 bytes
+//   partials          2 x NW x 8 x M floats
+struct BulkLayout {
+    int S, KS, NW;
+    long long x_off, x_stride, ring_off, row_stride, slot_bytes, red_off, total;
+    SK_HD BulkLayout(int M, int K, int KS_, int S_, int NW_) : S(S_), KS(KS_), NW(NW_) {
+        x_off = 256;
+        x_stride = 2LL * K + 16;
+        ring_off = x_off + M * x_stride;
+        row_stride = 2LL * KS + 16;
+        slot_bytes = 8 * row_stride;
+        red_off = ring_off + S * slot_bytes;
+        total = red_off + 2LL * NW * 8 * M * 4;
+    }
 };
 
 // A compiled instantiation of a kernel template.
@@ -45,7 +76,8 @@ struct KernelInfo {
     int M;
     int R;        // rows per lane group
     int LPR;      // lanes per row
-    int U;        // 16-byte loads per row per lane in flight
+    int U;        // loads (CUDA cores) or 32-element k-blocks (tensor cores) per batch
+    int stages;   // batches in flight: 1, or 2 when double-buffered
     const void *fn;
 };
 
@@ -68,5 +100,7 @@ size_t smem_bytes(const sgemm_plan_t &plan, int M, int kps);
 // for the tensor-core kernel) and the CTAs that can use them.
 int work_units(const sgemm_plan_t &plan, int N);
 long long ctas_wanted(const sgemm_plan_t &plan, int N);
+// Let a kernel use all the dynamic shared memory its static part leaves.
+cudaError_t allow_max_dynamic_smem(const void *fn);
 
 }  // namespace sk

@@ -13,8 +13,10 @@
 //    U loads at once and consuming them together.  Batches rather than a
 //    rolling ring: measured on GB300, a register ring of loads consumed one at
 //    a time keeps only about one load per warp in flight, while a batch keeps
-//    all U in flight (5.1 vs 1.3 TB/s at 8 warps per SM).  The number of bytes
-//    in flight therefore does not depend on K.
+//    all U in flight (5.1 vs 1.3 TB/s at 8 warps per SM).  With DB, two
+//    batches alternate between two register sets, the next one issued before
+//    the current one is consumed, so loads stay in flight while the warp
+//    computes.  The number of bytes in flight does not depend on K.
 //  * The first U loads are issued before x is staged, so the latency of the
 //    W stream and of the x staging overlap.
 //  * x (all M rows of this CTA's K range) is staged once per CTA in shared
@@ -142,7 +144,7 @@ struct XChunk<M, true> {
     }
 };
 
-template <int M, int R, int LPR, int U, bool MIX>
+template <int M, int R, int LPR, int U, bool MIX, bool DB>
 __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_constant__ Params p) {
     static_assert(LPR == 32 || LPR == 16 || LPR == 8, "lanes per row");
     constexpr int G = 32 / LPR;  // lane groups per warp
@@ -189,8 +191,8 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
     };
     rows_of(0);
 
-    uint4 buf[U][R];
-    auto issue_batch = [&](int base) {
+    using Batch = uint4[U][R];
+    auto issue_batch = [&](Batch &buf, int base) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (base + u < total) {
@@ -206,10 +208,11 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
         }
     };
 
+    Batch bufA, bufB;
     const bool early_w = !pdl || (p.flags & kFlagWeightsReadOnly);
-    if (early_w) issue_batch(0);
+    if (early_w) issue_batch(bufA, 0);
     if (pdl) pdl_wait();
-    if (!early_w) issue_batch(0);
+    if (!early_w) issue_batch(bufA, 0);
 
     // stage x[:, k0:k0+kc] in shared memory (overlaps the first batch's latency)
     for (int i = threadIdx.x; i < M * nchunk; i += blockDim.x) {
@@ -226,7 +229,7 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
         for (int r = 0; r < R; ++r) acc[m][r] = 0.0f;
 
     int ct = 0, cj = 0;
-    for (int base = 0; base < total; base += U) {
+    auto consume_batch = [&](const Batch &buf, int base) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (base + u < total) {
@@ -276,7 +279,24 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
                 }
             }
         }
-        if (base + U < total) issue_batch(base + U);
+    };
+
+    if (DB) {
+        // two batches in flight: the next batch is issued before the current one is
+        // consumed (the two buffers are distinct registers, so consuming one does not
+        // wait for the other's loads)
+        for (int base = 0; base < total; base += 2 * U) {
+            if (base + U < total) issue_batch(bufB, base + U);
+            consume_batch(bufA, base);
+            if (base + U >= total) break;
+            if (base + 2 * U < total) issue_batch(bufA, base + 2 * U);
+            consume_batch(bufB, base + U);
+        }
+    } else {
+        for (int base = 0; base < total; base += U) {
+            consume_batch(bufA, base);
+            if (base + U < total) issue_batch(bufA, base + U);
+        }
     }
 }
 

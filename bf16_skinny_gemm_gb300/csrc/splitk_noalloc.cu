@@ -12,9 +12,9 @@
 // device image and is created when the library's code is loaded on a device.
 //
 // The kernels are the regular ones of the selected plan (the streaming kernel
-// with gridDim.y splits, then splitk_reduce_kernel); only where the FP32
-// partial sums live differs, so results are bitwise equal to
-// sgemm_bf16_skinny_ex with the same plan and split.
+// with gridDim.y splits, then splitk_reduce_kernel; a CUDA-core plan when the
+// selected one cannot split K); only where the FP32 partial sums live differs,
+// so results are bitwise equal to sgemm_bf16_skinny_ex with that plan.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -51,9 +51,10 @@ const sk::KernelInfo *find(int M, const sgemm_plan_t &p) {
         case 4: t = sk::kKernelsM4; break;
         default: return nullptr;
     }
+    const int stages = p.stages == 0 ? 1 : p.stages;
     for (int i = 0; i < sk::kKernelCountPerM; ++i)
         if (t[i].variant == p.variant && t[i].R == p.rows_per_warp &&
-            t[i].LPR == p.lanes_per_row && t[i].U == p.k_unroll)
+            t[i].LPR == p.lanes_per_row && t[i].U == p.k_unroll && t[i].stages == stages)
             return &t[i];
     return nullptr;
 }
@@ -84,9 +85,7 @@ sgemm_status_t setup_current_device(DeviceSetup **out) {
                                               sk::kKernelsM4};
             for (const sk::KernelInfo *t : tables)
                 for (int i = 0; i < sk::kKernelCountPerM; ++i)
-                    if (cudaFuncSetAttribute(t[i].fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             227 * 1024) != cudaSuccess)
-                        return SGEMM_ERR_CUDA;
+                    if (sk::allow_max_dynamic_smem(t[i].fn) != cudaSuccess) return SGEMM_ERR_CUDA;
         }
         st.done = true;
     }
@@ -113,6 +112,16 @@ extern "C" sgemm_status_t sgemm_bf16_skinny_splitk_noalloc(
 
     sgemm_plan_t plan = sgemm_plan_select(N, K, M);
     plan.split_k = split_k;
+    if (plan.variant == SGEMM_VARIANT_BULK) {
+        // the bulk-copy kernel does not split K: use the CUDA-core streaming kernel
+        plan.variant = SGEMM_VARIANT_LDG_MIXFMA;
+        plan.threads = 256;
+        plan.rows_per_warp = 1;
+        plan.lanes_per_row = 32;
+        plan.k_unroll = 8;
+        plan.stages = 1;
+        plan.ctas_per_sm = 0;
+    }
     sgemm_status_t s = sgemm_plan_check(&plan, M, N, K);
     if (s != SGEMM_OK) return s;
     const sk::KernelInfo *ki = find(M, plan);

@@ -45,12 +45,19 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 DEFAULT_OUT = os.path.join(HERE, "csrc", "plan_table.inc")
 
 
+# bulk-copy kernel geometry: (stage width in 32-element k-blocks, ring slots)
+BULK_GEOMETRY = [(16, 8), (32, 4), (32, 6), (64, 2), (64, 3)]
+
+
 def candidates(M, N, K, splits):
     out = []
     for i in range(sk.sgemm_plan_count()):
         base = sk.sgemm_plan_get(i)
-        for s in splits:
-            p = base.copy(split_k=s)
+        if base.variant == sk.SGEMM_VARIANT_BULK:
+            variants = [base.copy(k_unroll=kb, stages=ring) for kb, ring in BULK_GEOMETRY]
+        else:
+            variants = [base.copy(split_k=s) for s in splits]
+        for p in variants:
             if sk.sgemm_plan_check(p, M, N, K) == sk.SGEMM_OK:
                 out.append(p)
     return out
@@ -114,8 +121,11 @@ def sweep_shape(N, K, Ms, splits, flags, trials, replays, min_bytes, pair=False,
         order = sorted(range(len(cands)), key=lambda i: med[i])
         best = cands[order[0]]
         nbytes = (2 if pair else 1) * 2 * (N * K + M * K + M * N)
-        heur_us = next((med[i] for i, p in enumerate(cands)
-                        if p.as_dict() == heur.as_dict()), None)
+        def same(a, b):
+            da, db = a.as_dict(), b.as_dict()
+            da.pop("id"), db.pop("id")
+            return da == db
+        heur_us = next((med[i] for i, p in enumerate(cands) if same(p, heur)), None)
         results[M] = {"plan": best.as_dict(), "us": med[order[0]],
                       "gbs": nbytes / med[order[0]] / 1e3,
                       "heuristic_us": heur_us,
@@ -133,7 +143,7 @@ def sweep_shape(N, K, Ms, splits, flags, trials, replays, min_bytes, pair=False,
 
 def _short(p):
     return (f"v{p.variant} t{p.threads} R{p.rows_per_warp} L{p.lanes_per_row} "
-            f"U{p.k_unroll} S{p.split_k}")
+            f"U{p.k_unroll}x{max(p.stages, 1)} S{p.split_k}")
 
 
 def write_table(entries, path, note):

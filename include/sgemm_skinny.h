@@ -80,7 +80,8 @@ typedef struct {
     int k_unroll;         /* 16-byte W loads per row per lane kept in flight */
     int vec_bytes;        /* bytes per W load: 16 */
     int split_k;          /* K split across this many CTAs (1 = none) */
-    int stages;           /* shared-memory pipeline depth (0 = register streaming) */
+    int stages;           /* pipeline depth: batches of loads in flight per warp, 1 or 2
+                             (2 = double-buffered batches; 0 is read as 1) */
     int ctas_per_sm;      /* resident CTAs per SM the grid is sized for (0 = occupancy max) */
     int id;               /* index in the compiled plan table, or -1 for a heuristic plan */
 } sgemm_plan_t;
@@ -91,11 +92,22 @@ enum {
                                      FP32 FMA, warp-shuffle reduction */
     SGEMM_VARIANT_LDG_MIXFMA = 1, /* the same with the mixed-precision FMA (BF16 operands, FP32
                                      addend): fewer instructions, bitwise-identical results */
-    SGEMM_VARIANT_MMA = 2         /* W streamed the same way into mma.sync m16n8k16 tensor-core
+    SGEMM_VARIANT_MMA = 2,        /* W streamed the same way into mma.sync m16n8k16 tensor-core
                                      fragments (x padded to 8 columns); a CTA of NW warps splits
                                      each 16-row tile's K range and adds the NW partial tiles in
                                      shared memory.  rows_per_warp = 16, lanes_per_row = 4,
                                      k_unroll = 32-element k-blocks per batch */
+    SGEMM_VARIANT_MMA_T = 3,      /* tensor cores with x as the A operand (rows m < M) and 8 rows
+                                     of W as the B operand: 8-row tiles, each lane streams 16 B of
+                                     one row per step.  rows_per_warp = 8, lanes_per_row = 4,
+                                     k_unroll = k-blocks per batch, stages = 1 or 2 batches */
+    SGEMM_VARIANT_BULK = 4        /* one persistent CTA per SM streams a balanced row range of W
+                                     with cp.async.bulk copies into an mbarrier-tracked ring of
+                                     shared-memory slots (a producer thread), consumer warps run
+                                     the x-as-A MMA on it.  threads = 32 * (1 + consumer warps),
+                                     rows_per_warp = 8, lanes_per_row = 4, k_unroll = stage width
+                                     in 32-element k-blocks, stages = ring slots (2..16),
+                                     split_k = 1.  Needs the library scratch for its error word */
 };
 
 /* Launch flags (bit set) for the _ex calls.
@@ -112,6 +124,10 @@ enum {
  *   kernel finishes. */
 #define SGEMM_FLAG_PDL 1u
 #define SGEMM_FLAG_WEIGHTS_READONLY 2u
+/* TEST ONLY: bulk-copy kernels (SGEMM_VARIANT_BULK) issue no copies, so their
+ * bounded waits run out (about 0.2 s); they then write NaN outputs, set the
+ * device error word and return.  Exercises failure detection without a fault. */
+#define SGEMM_FLAG_TEST_STALL 4u
 
 /* y = x . W^T for contiguous x [M,K] and y [M,N].  Plan: sgemm_plan_select(N, K, M). */
 sgemm_status_t sgemm_bf16_skinny(const sgemm_bf16_t *x, const sgemm_bf16_t *W, sgemm_bf16_t *y,
@@ -205,7 +221,9 @@ sgemm_status_t sgemm_bf16_rescale(const sgemm_bf16_t *y, long long n_src, sgemm_
  * the FP32 partial sums in a fixed, library-owned device array of
  * SGEMM_NOALLOC_SCRATCH_BYTES (4 MiB) instead of allocated scratch.
  * - The caller passes inputs and outputs as for sgemm_bf16_skinny_ex (device
- *   pointers, strides in elements); split_k must be >= 2.
+ *   pointers, strides in elements); split_k must be >= 2.  The selected plan
+ *   is used with split_k splits; when the selected plan cannot split K (the
+ *   bulk-copy variant), a CUDA-core streaming plan is used instead.
  * - split_k * M * N * 4 bytes must fit SGEMM_NOALLOC_SCRATCH_BYTES; larger
  *   problems return SGEMM_ERR_UNSUPPORTED_SHAPE and launch nothing.
  * - The first call on a device does a one-time set-up with that device current
@@ -221,6 +239,12 @@ sgemm_status_t sgemm_bf16_skinny_splitk_noalloc(const sgemm_bf16_t *x, long long
                                                 const sgemm_bf16_t *W, sgemm_bf16_t *y,
                                                 long long ldy, int M, int N, int K, int split_k,
                                                 sgemm_stream_t stream);
+
+/* Reads and clears the device error word of the current device: bit 0 is set
+ * when a bulk-copy kernel gave up waiting for its data (its outputs were
+ * written as NaN).  *flags = 0 when nothing went wrong or no such kernel ran.
+ * Synchronous (waits for the device); do not call during stream capture. */
+sgemm_status_t sgemm_device_errors(int *flags);
 
 /* Static description of a status code (never NULL). */
 const char *sgemm_status_string(sgemm_status_t status);

@@ -87,7 +87,7 @@ def test_bad_strides_and_alignment_rejected(lib):
 
 
 def test_unknown_flags_rejected(lib):
-    assert lib.sgemm_bf16_skinny_ex(A16, 64, A16, A16, 16, 1, 16, 64, None, 4, None) == \
+    assert lib.sgemm_bf16_skinny_ex(A16, 64, A16, A16, 16, 1, 16, 64, None, 8, None) == \
         sk.SGEMM_ERR_INVALID_ARG
     pairs = (sk.Pair * 1)()
     pairs[0].x, pairs[0].W, pairs[0].y, pairs[0].ldx, pairs[0].ldy = A16, A16, A16, 64, 16
@@ -110,7 +110,7 @@ def test_bad_plans_rejected(lib):
     good = sk.sgemm_plan_select(4096, 4096, 1)
     assert sk.sgemm_plan_check(good, 1, 4096, 4096) == sk.SGEMM_OK
     for change in ({"variant": 7}, {"variant": -1}, {"threads": 48}, {"threads": 512}, {"vec_bytes": 8},
-                   {"split_k": 0}, {"k_unroll": 3}, {"lanes_per_row": 4}, {"stages": 2}):
+                   {"split_k": 0}, {"k_unroll": 3}, {"lanes_per_row": 4}, {"stages": 3}):
         bad = good.copy(**change)
         assert sk.sgemm_plan_check(bad, 1, 4096, 4096) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE, change
         assert _call_plan(lib, bad) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE, change

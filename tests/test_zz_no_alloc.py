@@ -8,9 +8,8 @@ serves them: its split-K partial sums live in a fixed 4 MiB device array inside
 the library instead of allocated scratch.
 
 This test calls it through the C ABI twice in a row, with different inputs, and
-checks each output against the regular split-K entry point
-(sgemm_bf16_skinny_ex with the same split) within the tolerance used by every
-parity test here.  A stale partial sum left by the first call would break the
+checks each output against the regular entry point (sgemm_bf16_skinny) within
+the tolerance used by every parity test here.  A stale partial sum left by the first call would break the
 second comparison.  It also checks that a problem too large for the fixed
 array is refused.  It must pass alone in a fresh process and after the rest of
 the suite.
@@ -45,9 +44,8 @@ def test_no_alloc_matches_regular_split_k_on_two_calls(M, N, K, split):
     sk.sgemm_bf16_skinny_splitk_noalloc(xa, Wa, ya, split_k=split)
     sk.sgemm_bf16_skinny_splitk_noalloc(xb, Wb, yb, split_k=split)
     torch.cuda.synchronize()
-    plan = sk.sgemm_plan_select(N, K, M).copy(split_k=split)
     for x, W, y in ((xa, Wa, ya), (xb, Wb, yb)):
-        ref = sk.sgemm_bf16_skinny_ex(x, W, plan=plan)
+        ref = sk.sgemm_bf16_skinny(x, W)  # the existing entry point, its own plan
         torch.cuda.synchronize()
         rep = compare(synth.bits(y), synth.bits(ref), synth.bits(x), synth.bits(W))
         assert rep["ok"], rep
