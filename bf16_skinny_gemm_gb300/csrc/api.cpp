@@ -98,7 +98,8 @@ sgemm_status_t check_plan(const sgemm_plan_t &p, int M, int N, int K) {
     (void)N;
     if (p.variant == SGEMM_VARIANT_BULK) return check_bulk_plan(p, M, K);
     if (p.variant != SGEMM_VARIANT_LDG && p.variant != SGEMM_VARIANT_LDG_MIXFMA &&
-        p.variant != SGEMM_VARIANT_MMA && p.variant != SGEMM_VARIANT_MMA_T)
+        p.variant != SGEMM_VARIANT_LDG_FFMA2 && p.variant != SGEMM_VARIANT_MMA &&
+        p.variant != SGEMM_VARIANT_MMA_T)
         return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.threads < 32 || p.threads > sk::kMaxThreads || p.threads % 32) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.vec_bytes != 16 || p.stages < 0 || p.stages > 2) return SGEMM_ERR_UNSUPPORTED_SHAPE;

@@ -1,7 +1,7 @@
 // The compiled configurations of the weight-streaming kernel.  Each line is
-// (M, rows per lane group R, lanes per row LPR, loads per batch U,
-// mixed-precision FMA, double-buffered batches); every configuration exists
-// for M = 1..4.  The host
+// (M, rows per lane group R, lanes per row LPR, loads per batch U, FMA mode
+// (0 widened, 1 mixed precision, 2 packed FP32x2), double-buffered batches);
+// every configuration exists for M = 1..4.  The host
 // library enumerates these as plans (times two CTA sizes) and the offline
 // sweep times all of them.
 #pragma once
@@ -11,27 +11,34 @@
 #include "skinny_mmat.cuh"
 #include "skinny_bulk.cuh"
 
-#define SK_LDG_CONFIGS(X, M)        \
-    X(M, 1, 32, 8, false, false)    \
-    X(M, 1, 32, 8, true, false)     \
-    X(M, 1, 32, 4, true, false)     \
-    X(M, 2, 32, 2, true, false)     \
-    X(M, 2, 32, 4, true, false)     \
-    X(M, 4, 32, 2, true, false)     \
-    X(M, 2, 16, 2, true, false)     \
-    X(M, 1, 16, 4, true, false)     \
-    X(M, 4, 8, 2, true, false)      \
-    X(M, 1, 32, 4, true, true)      \
-    X(M, 1, 32, 8, true, true)      \
-    X(M, 2, 32, 2, true, true)      \
-    X(M, 2, 32, 4, true, true)      \
-    X(M, 4, 32, 2, true, true)      \
-    X(M, 1, 16, 4, true, true)      \
-    X(M, 2, 16, 2, true, true)
+#define SK_LDG_CONFIGS(X, M)   \
+    X(M, 1, 32, 8, 0, false)   \
+    X(M, 1, 32, 8, 1, false)   \
+    X(M, 1, 32, 4, 1, false)   \
+    X(M, 2, 32, 2, 1, false)   \
+    X(M, 2, 32, 4, 1, false)   \
+    X(M, 4, 32, 2, 1, false)   \
+    X(M, 2, 16, 2, 1, false)   \
+    X(M, 1, 16, 4, 1, false)   \
+    X(M, 4, 8, 2, 1, false)    \
+    X(M, 1, 32, 4, 1, true)    \
+    X(M, 2, 32, 2, 1, true)    \
+    X(M, 2, 16, 2, 1, true)    \
+    X(M, 1, 32, 8, 2, false)   \
+    X(M, 2, 32, 4, 2, false)   \
+    X(M, 4, 32, 2, 2, false)   \
+    X(M, 2, 32, 2, 2, false)   \
+    X(M, 4, 32, 4, 2, false)   \
+    X(M, 2, 16, 2, 2, false)   \
+    X(M, 1, 16, 4, 2, false)   \
+    X(M, 4, 8, 2, 2, false)    \
+    X(M, 2, 32, 2, 2, true)
 
-#define SK_LDG_ENTRY(M, R, LPR, U, MIX, DB)                                              \
-    {(MIX) ? SGEMM_VARIANT_LDG_MIXFMA : SGEMM_VARIANT_LDG, M, R, LPR, U, (DB) ? 2 : 1,   \
-     reinterpret_cast<const void *>(&skinny_ldg_kernel<M, R, LPR, U, MIX, DB>)},
+#define SK_LDG_ENTRY(M, R, LPR, U, FMODE, DB)                                              \
+    {(FMODE) == 2 ? SGEMM_VARIANT_LDG_FFMA2                                               \
+                  : ((FMODE) == 1 ? SGEMM_VARIANT_LDG_MIXFMA : SGEMM_VARIANT_LDG),        \
+     M, R, LPR, U, (DB) ? 2 : 1,                                                          \
+     reinterpret_cast<const void *>(&skinny_ldg_kernel<M, R, LPR, U, FMODE, DB>)},
 
 // Tensor-core configurations: (M, k-blocks per batch U).  R = 16 rows per tile,
 // 4 lanes share a row segment.

@@ -24,9 +24,8 @@
 //  * A warp is split into 32/LPR lane groups; each group owns R rows at a time
 //    and walks their K range with stride LPR chunks of 8 elements.  Each lane
 //    keeps M*R FP32 accumulators.  Products are exact in FP32 and are added
-//    with FMA: either after widening both BF16 operands to FP32 (MIX = false)
-//    or with the sm_100+ mixed-precision FMA that takes BF16 operands and an
-//    FP32 addend directly (MIX = true); both round once per addition to FP32.
+//    with FMA (see XChunk: widened FMA, mixed-precision FMA, or packed FP32x2
+//    FMA over even/odd k).
 //  * Lane partial sums are combined with an xor-butterfly of warp shuffles
 //    (fixed order).  With split-K (gridDim.y > 1) each split writes FP32
 //    partials and a second kernel adds them in split order.
@@ -37,9 +36,9 @@
 //    reads x or writes y (and, unless told that W is read-only with respect to
 //    the previous kernel, before it reads W).
 //
-// Accumulation order for one output is a function of (K range, LPR) only: it
-// never depends on M, R, U, MIX, the CTA size or the grid, which makes results
-// deterministic and row-wise independent of M.
+// Accumulation order for one output is a function of (K range, LPR, FMODE
+// pairing) only: it never depends on M, R, U, the CTA size or the grid, which
+// makes results deterministic and row-wise independent of M.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -85,14 +84,23 @@ __device__ __forceinline__ float fma2_bf16(uint32_t xw, uint32_t ww, float acc) 
     return acc;
 }
 
-// x operand of one chunk (8 elements) for all M rows: widened to FP32, or kept
-// as packed BF16 pairs for the mixed-precision FMA.
-template <int M, bool MIX>
+// x operand of one chunk (8 elements) for all M rows, and how a chunk of W is
+// multiplied into the accumulators.  FMODE selects the arithmetic:
+//   0: widen both operands to FP32, one FMA per element;
+//   1: the mixed-precision FMA (BF16 operands, FP32 addend) per element;
+//   2: packed FP32x2 FMA (fma.rn.f32x2, sm_100+): each accumulator is a pair
+//      {even k, odd k} of FP32 partial sums, one instruction per two elements;
+//      the pair is added (even + odd) when the row is finished.
+// Modes 0 and 1 round identically (one rounding per element); mode 2 keeps two
+// partial sums and so a different, equally fixed, summation order.
+template <int M, int FMODE>
 struct XChunk;
 
 template <int M>
-struct XChunk<M, false> {
+struct XChunk<M, 0> {
+    using Acc = float;
     float v[M][8];
+    static __device__ __forceinline__ float total(Acc a) { return a; }
     __device__ __forceinline__ void load(const uint4 *xs, int nchunk, int c) {
 #pragma unroll
         for (int m = 0; m < M; ++m) {
@@ -106,7 +114,7 @@ struct XChunk<M, false> {
         }
     }
     template <int R>
-    __device__ __forceinline__ void fma(float (&acc)[M][R], const uint4 &w, int r) const {
+    __device__ __forceinline__ void fma(Acc (&acc)[M][R], const uint4 &w, int r) const {
         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -122,8 +130,10 @@ struct XChunk<M, false> {
 };
 
 template <int M>
-struct XChunk<M, true> {
+struct XChunk<M, 1> {
+    using Acc = float;
     uint32_t v[M][4];
+    static __device__ __forceinline__ float total(Acc a) { return a; }
     __device__ __forceinline__ void load(const uint4 *xs, int nchunk, int c) {
 #pragma unroll
         for (int m = 0; m < M; ++m) {
@@ -135,7 +145,7 @@ struct XChunk<M, true> {
         }
     }
     template <int R>
-    __device__ __forceinline__ void fma(float (&acc)[M][R], const uint4 &w, int r) const {
+    __device__ __forceinline__ void fma(Acc (&acc)[M][R], const uint4 &w, int r) const {
         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -144,7 +154,49 @@ struct XChunk<M, true> {
     }
 };
 
-template <int M, int R, int LPR, int U, bool MIX, bool DB>
+// {lo, hi} FP32 pair in one 64-bit register pair
+__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
+                                                   unsigned long long c) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(c) : "l"(a), "l"(b));
+    return c;
+}
+
+template <int M>
+struct XChunk<M, 2> {
+    using Acc = unsigned long long;  // {sum over even k, sum over odd k}
+    unsigned long long v[M][4];
+    static __device__ __forceinline__ float total(Acc a) {
+        float lo, hi;
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+        return lo + hi;
+    }
+    __device__ __forceinline__ void load(const uint4 *xs, int nchunk, int c) {
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            const uint4 q = xs[m * nchunk + c];
+            const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[m][i] = pack_f32x2(bf16_lo(qq[i]), bf16_hi(qq[i]));
+        }
+    }
+    template <int R>
+    __device__ __forceinline__ void fma(Acc (&acc)[M][R], const uint4 &w, int r) const {
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const unsigned long long wp = pack_f32x2(bf16_lo(ww[i]), bf16_hi(ww[i]));
+#pragma unroll
+            for (int m = 0; m < M; ++m) acc[m][r] = ffma2(v[m][i], wp, acc[m][r]);
+        }
+    }
+};
+
+template <int M, int R, int LPR, int U, int FMODE, bool DB>
 __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_constant__ Params p) {
     static_assert(LPR == 32 || LPR == 16 || LPR == 8, "lanes per row");
     constexpr int G = 32 / LPR;  // lane groups per warp
@@ -222,11 +274,13 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
     }
     __syncthreads();
 
-    float acc[M][R];
+    using XC = XChunk<M, FMODE>;
+    using Acc = typename XC::Acc;
+    Acc acc[M][R];
 #pragma unroll
     for (int m = 0; m < M; ++m)
 #pragma unroll
-        for (int r = 0; r < R; ++r) acc[m][r] = 0.0f;
+        for (int r = 0; r < R; ++r) acc[m][r] = Acc(0);
 
     int ct = 0, cj = 0;
     auto consume_batch = [&](const Batch &buf, int base) {
@@ -234,22 +288,23 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
         for (int u = 0; u < U; ++u) {
             if (base + u < total) {
                 if ((cj < jtot - 1) || (li < last_lanes)) {
-                    XChunk<M, MIX> xc;
+                    XC xc;
                     xc.load(xs, nchunk, li + LPR * cj);
 #pragma unroll
                     for (int r = 0; r < R; ++r) xc.template fma<R>(acc, buf[u][r], r);
                 }
                 if (++cj == jtot) {
                     // task done: xor-butterfly over the LPR lanes (fixed tree order)
+                    float tot[M][R];
 #pragma unroll
                     for (int m = 0; m < M; ++m)
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
-                            float v = acc[m][r];
+                            float v = XC::total(acc[m][r]);
 #pragma unroll
                             for (int off = LPR / 2; off >= 1; off >>= 1)
                                 v += __shfl_xor_sync(0xffffffffu, v, off);
-                            acc[m][r] = v;
+                            tot[m][r] = v;
                         }
                     if (li == 0) {
                         const int n0 = ((g0 + ct * warps) * G + gi) * R;
@@ -260,11 +315,11 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
 #pragma unroll
                                 for (int m = 0; m < M; ++m) {
                                     if (p.split == 1) {
-                                        it.y[m * it.ldy + n] = f32_to_bf16_rn(acc[m][r]);
+                                        it.y[m * it.ldy + n] = f32_to_bf16_rn(tot[m][r]);
                                     } else {
                                         const long long slot =
                                             (static_cast<long long>(blockIdx.z) * p.split + s) * M + m;
-                                        p.ws[slot * p.N + n] = acc[m][r];
+                                        p.ws[slot * p.N + n] = tot[m][r];
                                     }
                                 }
                             }
@@ -273,7 +328,7 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
 #pragma unroll
                     for (int m = 0; m < M; ++m)
 #pragma unroll
-                        for (int r = 0; r < R; ++r) acc[m][r] = 0.0f;
+                        for (int r = 0; r < R; ++r) acc[m][r] = Acc(0);
                     cj = 0;
                     ++ct;
                 }

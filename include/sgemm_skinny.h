@@ -101,13 +101,16 @@ enum {
                                      of W as the B operand: 8-row tiles, each lane streams 16 B of
                                      one row per step.  rows_per_warp = 8, lanes_per_row = 4,
                                      k_unroll = k-blocks per batch, stages = 1 or 2 batches */
-    SGEMM_VARIANT_BULK = 4        /* one persistent CTA per SM streams a balanced row range of W
+    SGEMM_VARIANT_BULK = 4,       /* one persistent CTA per SM streams a balanced row range of W
                                      with cp.async.bulk copies into an mbarrier-tracked ring of
                                      shared-memory slots (a producer thread), consumer warps run
                                      the x-as-A MMA on it.  threads = 32 * (1 + consumer warps),
                                      rows_per_warp = 8, lanes_per_row = 4, k_unroll = stage width
                                      in 32-element k-blocks, stages = ring slots (2..16),
                                      split_k = 1.  Needs the library scratch for its error word */
+    SGEMM_VARIANT_LDG_FFMA2 = 5   /* the streaming kernel of variant 0 with packed FP32x2 FMA
+                                     (two partial sums per output, even and odd k, added at the
+                                     end): half the FMA instructions */
 };
 
 /* Launch flags (bit set) for the _ex calls.

@@ -329,8 +329,9 @@ def test_batched_graph_replay():
 @pytest.mark.parametrize("M", [1, 3, 4])
 def test_plans_with_same_lanes_per_row_agree_bitwise(M):
     """For the CUDA-core kernels the accumulation order depends only on (K range,
-    lanes per row): the mixed-precision FMA and the widened FP32 FMA, any R, U
-    and CTA size must give the same bits.  For the tensor-core and bulk kernels
+    lanes per row, FMA pairing): the mixed-precision FMA and the widened FP32
+    FMA, any R, U and CTA size must give the same bits (and so must any packed
+    FP32x2 plans among themselves).  For the tensor-core and bulk kernels
     it depends on (K range, warps per CTA): any U and batch depth must give the
     same bits."""
     N, K = 1500, 3072
@@ -346,8 +347,10 @@ def test_plans_with_same_lanes_per_row_agree_bitwise(M):
             torch.cuda.synchronize()
             mma = plan.variant in (sk.SGEMM_VARIANT_MMA, sk.SGEMM_VARIANT_MMA_T,
                                    sk.SGEMM_VARIANT_BULK)
-            key = (plan.variant if mma else -1, plan.lanes_per_row, split,
-                   plan.threads if mma else 0)
+            # the widened and the mixed-precision FMA round identically; the packed
+            # FP32x2 FMA keeps two partial sums, a different order of its own
+            fam = plan.variant if (mma or plan.variant == sk.SGEMM_VARIANT_LDG_FFMA2) else -1
+            key = (fam, plan.lanes_per_row, split, plan.threads if mma else 0)
             if key in by_lpr:
                 assert torch.equal(by_lpr[key][1].view(torch.int16), y.view(torch.int16)), \
                     (by_lpr[key][0], plan)
