@@ -99,7 +99,8 @@ sgemm_status_t check_plan(const sgemm_plan_t &p, int M, int N, int K) {
     if (p.variant == SGEMM_VARIANT_BULK) return check_bulk_plan(p, M, K);
     if (p.variant != SGEMM_VARIANT_LDG && p.variant != SGEMM_VARIANT_LDG_MIXFMA &&
         p.variant != SGEMM_VARIANT_LDG_FFMA2 && p.variant != SGEMM_VARIANT_MMA &&
-        p.variant != SGEMM_VARIANT_MMA_T)
+        p.variant != SGEMM_VARIANT_MMA_T && p.variant != SGEMM_VARIANT_LDGX_MIXFMA &&
+        p.variant != SGEMM_VARIANT_LDGX_FFMA2)
         return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.threads < 32 || p.threads > sk::kMaxThreads || p.threads % 32) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.vec_bytes != 16 || p.stages < 0 || p.stages > 2) return SGEMM_ERR_UNSUPPORTED_SHAPE;
@@ -363,6 +364,8 @@ size_t smem_bytes(const sgemm_plan_t &plan, int M, int kps) {
         return static_cast<size_t>(L.total);
     }
     const size_t chunks = static_cast<size_t>(kps) / 8;
+    if (plan.variant == SGEMM_VARIANT_LDGX_MIXFMA || plan.variant == SGEMM_VARIANT_LDGX_FFMA2)
+        return 0;  // x is read from global memory
     if (plan.variant == SGEMM_VARIANT_MMA) {
         // x rows padded by one chunk, plus two reduction buffers [NW][16][4] floats
         return static_cast<size_t>(M) * (chunks + 1) * 16 +

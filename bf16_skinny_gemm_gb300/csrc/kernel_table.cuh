@@ -34,6 +34,22 @@
     X(M, 4, 8, 2, 2, false)    \
     X(M, 2, 32, 2, 2, true)
 
+// The same kernel reading x straight from global memory (no staging): (M, R,
+// LPR, U, FMA mode).
+#define SK_LDGX_CONFIGS(X, M)  \
+    X(M, 1, 32, 8, 1)          \
+    X(M, 2, 32, 4, 1)          \
+    X(M, 4, 32, 2, 1)          \
+    X(M, 2, 32, 2, 1)          \
+    X(M, 1, 32, 4, 1)          \
+    X(M, 2, 16, 2, 1)          \
+    X(M, 4, 32, 2, 2)          \
+    X(M, 2, 32, 4, 2)
+
+#define SK_LDGX_ENTRY(M, R, LPR, U, FMODE)                                                 \
+    {(FMODE) == 2 ? SGEMM_VARIANT_LDGX_FFMA2 : SGEMM_VARIANT_LDGX_MIXFMA, M, R, LPR, U, 1, \
+     reinterpret_cast<const void *>(&skinny_ldg_kernel<M, R, LPR, U, FMODE, false, true>)},
+
 #define SK_LDG_ENTRY(M, R, LPR, U, FMODE, DB)                                              \
     {(FMODE) == 2 ? SGEMM_VARIANT_LDG_FFMA2                                               \
                   : ((FMODE) == 1 ? SGEMM_VARIANT_LDG_MIXFMA : SGEMM_VARIANT_LDG),        \
@@ -71,4 +87,5 @@
 
 #define SK_DEFINE_TABLE(M, NAME)                                                          \
     const KernelInfo NAME[] = {SK_LDG_CONFIGS(SK_LDG_ENTRY, M) SK_MMA_CONFIGS(SK_MMA_ENTRY, M) \
-                                   SK_MMAT_CONFIGS(SK_MMAT_ENTRY, M) SK_BULK_ENTRY(M)};
+                                   SK_MMAT_CONFIGS(SK_MMAT_ENTRY, M) SK_BULK_ENTRY(M)     \
+                                       SK_LDGX_CONFIGS(SK_LDGX_ENTRY, M)};

@@ -84,6 +84,14 @@ __device__ __forceinline__ float fma2_bf16(uint32_t xw, uint32_t ww, float acc) 
     return acc;
 }
 
+// 16 bytes of x: from shared memory (staged), or straight from global memory
+// through the L1 cache (x is a few KiB and stays there after the first touch).
+template <bool XG>
+__device__ __forceinline__ uint4 load_x(const uint4 *p) {
+    if (XG) return __ldg(p);
+    return *p;
+}
+
 // x operand of one chunk (8 elements) for all M rows, and how a chunk of W is
 // multiplied into the accumulators.  FMODE selects the arithmetic:
 //   0: widen both operands to FP32, one FMA per element;
@@ -101,10 +109,11 @@ struct XChunk<M, 0> {
     using Acc = float;
     float v[M][8];
     static __device__ __forceinline__ float total(Acc a) { return a; }
-    __device__ __forceinline__ void load(const uint4 *xs, int nchunk, int c) {
+    template <bool XG>
+    __device__ __forceinline__ void load(const uint4 *xs, long long stride, int c) {
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-            const uint4 q = xs[m * nchunk + c];
+            const uint4 q = load_x<XG>(xs + m * stride + c);
             const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -134,10 +143,11 @@ struct XChunk<M, 1> {
     using Acc = float;
     uint32_t v[M][4];
     static __device__ __forceinline__ float total(Acc a) { return a; }
-    __device__ __forceinline__ void load(const uint4 *xs, int nchunk, int c) {
+    template <bool XG>
+    __device__ __forceinline__ void load(const uint4 *xs, long long stride, int c) {
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-            const uint4 q = xs[m * nchunk + c];
+            const uint4 q = load_x<XG>(xs + m * stride + c);
             v[m][0] = q.x;
             v[m][1] = q.y;
             v[m][2] = q.z;
@@ -175,10 +185,11 @@ struct XChunk<M, 2> {
         asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
         return lo + hi;
     }
-    __device__ __forceinline__ void load(const uint4 *xs, int nchunk, int c) {
+    template <bool XG>
+    __device__ __forceinline__ void load(const uint4 *xs, long long stride, int c) {
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-            const uint4 q = xs[m * nchunk + c];
+            const uint4 q = load_x<XG>(xs + m * stride + c);
             const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) v[m][i] = pack_f32x2(bf16_lo(qq[i]), bf16_hi(qq[i]));
@@ -196,7 +207,7 @@ struct XChunk<M, 2> {
     }
 };
 
-template <int M, int R, int LPR, int U, int FMODE, bool DB>
+template <int M, int R, int LPR, int U, int FMODE, bool DB, bool XG = false>
 __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_constant__ Params p) {
     static_assert(LPR == 32 || LPR == 16 || LPR == 8, "lanes per row");
     constexpr int G = 32 / LPR;  // lane groups per warp
@@ -266,13 +277,18 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
     if (pdl) pdl_wait();
     if (!early_w) issue_batch(bufA, 0);
 
-    // stage x[:, k0:k0+kc] in shared memory (overlaps the first batch's latency)
-    for (int i = threadIdx.x; i < M * nchunk; i += blockDim.x) {
-        const int m = i / nchunk;
-        const int c = i - m * nchunk;
-        xs[i] = *reinterpret_cast<const uint4 *>(it.x + m * it.ldx + k0 + 8 * c);
+    // x: staged in shared memory (overlaps the first batch's latency), or read
+    // from global memory at each use (no staging, no CTA barrier)
+    const uint4 *xsrc = XG ? reinterpret_cast<const uint4 *>(it.x + k0) : xs;
+    const long long xstride = XG ? it.ldx / 8 : nchunk;
+    if (!XG) {
+        for (int i = threadIdx.x; i < M * nchunk; i += blockDim.x) {
+            const int m = i / nchunk;
+            const int c = i - m * nchunk;
+            xs[i] = *reinterpret_cast<const uint4 *>(it.x + m * it.ldx + k0 + 8 * c);
+        }
+        __syncthreads();
     }
-    __syncthreads();
 
     using XC = XChunk<M, FMODE>;
     using Acc = typename XC::Acc;
@@ -289,7 +305,7 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
             if (base + u < total) {
                 if ((cj < jtot - 1) || (li < last_lanes)) {
                     XC xc;
-                    xc.load(xs, nchunk, li + LPR * cj);
+                    xc.template load<XG>(xsrc, xstride, li + LPR * cj);
 #pragma unroll
                     for (int r = 0; r < R; ++r) xc.template fma<R>(acc, buf[u][r], r);
                 }

@@ -108,9 +108,13 @@ enum {
                                      rows_per_warp = 8, lanes_per_row = 4, k_unroll = stage width
                                      in 32-element k-blocks, stages = ring slots (2..16),
                                      split_k = 1.  Needs the library scratch for its error word */
-    SGEMM_VARIANT_LDG_FFMA2 = 5   /* the streaming kernel of variant 0 with packed FP32x2 FMA
+    SGEMM_VARIANT_LDG_FFMA2 = 5,  /* the streaming kernel of variant 0 with packed FP32x2 FMA
                                      (two partial sums per output, even and odd k, added at the
                                      end): half the FMA instructions */
+    SGEMM_VARIANT_LDGX_MIXFMA = 6, /* variant 1 reading x from global memory through L1 at each
+                                     use instead of staging it in shared memory (no CTA barrier
+                                     before the first FMA); same results as variants 0/1 */
+    SGEMM_VARIANT_LDGX_FFMA2 = 7  /* variant 5 with x read the same way; same results as 5 */
 };
 
 /* Launch flags (bit set) for the _ex calls.

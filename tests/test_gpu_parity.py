@@ -349,7 +349,8 @@ def test_plans_with_same_lanes_per_row_agree_bitwise(M):
                                    sk.SGEMM_VARIANT_BULK)
             # the widened and the mixed-precision FMA round identically; the packed
             # FP32x2 FMA keeps two partial sums, a different order of its own
-            fam = plan.variant if (mma or plan.variant == sk.SGEMM_VARIANT_LDG_FFMA2) else -1
+            ffma2 = plan.variant in (sk.SGEMM_VARIANT_LDG_FFMA2, sk.SGEMM_VARIANT_LDGX_FFMA2)
+            fam = plan.variant if mma else (5 if ffma2 else -1)
             key = (fam, plan.lanes_per_row, split, plan.threads if mma else 0)
             if key in by_lpr:
                 assert torch.equal(by_lpr[key][1].view(torch.int16), y.view(torch.int16)), \
