@@ -56,15 +56,19 @@
      M, R, LPR, U, (DB) ? 2 : 1,                                                          \
      reinterpret_cast<const void *>(&skinny_ldg_kernel<M, R, LPR, U, FMODE, DB>)},
 
-// Tensor-core configurations: (M, k-blocks per batch U).  R = 16 rows per tile,
-// 4 lanes share a row segment.
+// Tensor-core configurations: (M, k-blocks per batch U, double-buffered).
+// R = 16 rows per tile, 4 lanes share a row segment.
 #define SK_MMA_CONFIGS(X, M) \
-    X(M, 2)                  \
-    X(M, 4)                  \
-    X(M, 8)
+    X(M, 2, false)           \
+    X(M, 4, false)           \
+    X(M, 8, false)           \
+    X(M, 1, true)            \
+    X(M, 2, true)            \
+    X(M, 4, true)
 
-#define SK_MMA_ENTRY(M, U) \
-    {SGEMM_VARIANT_MMA, M, 16, 4, U, 1, reinterpret_cast<const void *>(&skinny_mma_kernel<M, U>)},
+#define SK_MMA_ENTRY(M, U, DB)                          \
+    {SGEMM_VARIANT_MMA, M, 16, 4, U, (DB) ? 2 : 1,      \
+     reinterpret_cast<const void *>(&skinny_mma_kernel<M, U, DB>)},
 
 // Tensor-core configurations with x as the A operand: (M, U, double-buffered).
 // R = 8 rows per tile, 4 lanes share a row segment.

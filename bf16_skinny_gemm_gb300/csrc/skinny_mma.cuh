@@ -21,7 +21,9 @@
 //    k-blocks w, w+NW, w+2NW, ... (the CTA sweeps each row contiguously), and
 //    the NW partial tiles are added in shared memory in warp order.
 //  * loads are issued in batches of U k-blocks (2U loads per lane) over the
-//    warp's flat sequence of (tile, k-block) steps, consumed together.
+//    warp's flat sequence of (tile, k-block) steps, consumed together; with DB
+//    two batches alternate, so a batch is in flight during the tile-end
+//    barrier and reduction.
 //
 // The order of accumulation depends on (K range, NW) only, never on M, so the
 // result is deterministic and row-wise independent of M for a given plan.
@@ -42,7 +44,7 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <int M, int U>
+template <int M, int U, bool DB = false>
 __global__ void __launch_bounds__(kMaxThreads) skinny_mma_kernel(const __grid_constant__ Params p) {
     constexpr int TILE = 16;
     extern __shared__ uint4 smem[];
@@ -83,15 +85,17 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mma_kernel(const __grid_co
     };
     if (total > 0) rows_of(lt);
 
-    uint4 wlo[U], whi[U];
-    auto issue_batch = [&](int base) {
+    struct Batch {
+        uint4 lo[U], hi[U];
+    };
+    auto issue_batch = [&](Batch &b, int base) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (base + u < total) {
                 const int jb = warp + li_ * NW;
                 const bool ok = jb < J && (4 * jb + c) < nchunk;
-                wlo[u] = ok ? ldg_stream(row_lo + 32 * jb) : make_uint4(0u, 0u, 0u, 0u);
-                whi[u] = ok ? ldg_stream(row_hi + 32 * jb) : make_uint4(0u, 0u, 0u, 0u);
+                b.lo[u] = ok ? ldg_stream(row_lo + 32 * jb) : make_uint4(0u, 0u, 0u, 0u);
+                b.hi[u] = ok ? ldg_stream(row_hi + 32 * jb) : make_uint4(0u, 0u, 0u, 0u);
                 if (++li_ == I) {
                     li_ = 0;
                     if (++lt < t_end) rows_of(lt);
@@ -100,10 +104,11 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mma_kernel(const __grid_co
         }
     };
 
+    Batch bA, bB;
     const bool early_w = !pdl || (p.flags & kFlagWeightsReadOnly);
-    if (early_w) issue_batch(0);
+    if (early_w) issue_batch(bA, 0);
     if (pdl) pdl_wait();
-    if (!early_w) issue_batch(0);
+    if (!early_w) issue_batch(bA, 0);
 
     for (int i = threadIdx.x; i < M * nchunk; i += blockDim.x) {
         const int m = i / nchunk;
@@ -114,7 +119,7 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mma_kernel(const __grid_co
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     int ct = t_begin, ci = 0, rb = 0;  // consume cursor: tile, step, reduction buffer
-    for (int base = 0; base < total; base += U) {
+    auto consume_batch = [&](const Batch &b, int base) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (base + u < total) {
@@ -122,8 +127,8 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mma_kernel(const __grid_co
                 if (jb < J) {
                     uint4 xv = make_uint4(0u, 0u, 0u, 0u);
                     if (g < M && (4 * jb + c) < nchunk) xv = xs[g * xstride + 4 * jb + c];
-                    const uint32_t a0[4] = {wlo[u].x, whi[u].x, wlo[u].y, whi[u].y};
-                    const uint32_t a1[4] = {wlo[u].z, whi[u].z, wlo[u].w, whi[u].w};
+                    const uint32_t a0[4] = {b.lo[u].x, b.hi[u].x, b.lo[u].y, b.hi[u].y};
+                    const uint32_t a1[4] = {b.lo[u].z, b.hi[u].z, b.lo[u].w, b.hi[u].w};
                     mma_bf16_16816(acc, a0, xv.x, xv.y);
                     mma_bf16_16816(acc, a1, xv.z, xv.w);
                 }
@@ -164,7 +169,23 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mma_kernel(const __grid_co
                 }
             }
         }
-        if (base + U < total) issue_batch(base + U);
+    };
+
+    if (DB) {
+        // the next batch is in flight while this one is consumed, including the
+        // tile-end barrier and reduction
+        for (int base = 0; base < total; base += 2 * U) {
+            if (base + U < total) issue_batch(bB, base + U);
+            consume_batch(bA, base);
+            if (base + U >= total) break;
+            if (base + 2 * U < total) issue_batch(bA, base + 2 * U);
+            consume_batch(bB, base + U);
+        }
+    } else {
+        for (int base = 0; base < total; base += U) {
+            consume_batch(bA, base);
+            if (base + U < total) issue_batch(bA, base + U);
+        }
     }
 }
 

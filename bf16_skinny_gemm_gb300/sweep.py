@@ -130,6 +130,7 @@ def sweep_shape(N, K, Ms, splits, flags, trials, replays, min_bytes, pair=False,
                       "gbs": nbytes / med[order[0]] / 1e3,
                       "heuristic_us": heur_us,
                       "top": [(cands[i].as_dict(), round(med[i], 3)) for i in order[:5]],
+                      "all": [(cands[i].as_dict(), round(med[i], 3)) for i in order],
                       "copies": R, "candidates": len(cands)}
         log(f"  N={N} K={K} M={M}: best {med[order[0]]:.3f} us "
             f"({results[M]['gbs']:.0f} GB/s) {_short(best)}; heuristic "
@@ -144,6 +145,27 @@ def sweep_shape(N, K, Ms, splits, flags, trials, replays, min_bytes, pair=False,
 def _short(p):
     return (f"v{p.variant} t{p.threads} R{p.rows_per_warp} L{p.lanes_per_row} "
             f"U{p.k_unroll}x{max(p.stages, 1)} S{p.split_k}")
+
+
+def read_table(path):
+    """Entries of an existing generated table: {(N, K, M): {"plan": ..., "us", "gbs"}}."""
+    out = {}
+    keys = ["variant", "threads", "rows_per_warp", "lanes_per_row", "k_unroll", "split_k",
+            "stages", "ctas_per_sm"]
+    with open(path) as f:
+        for ln in f:
+            ln = ln.strip()
+            if not ln.startswith("{"):
+                continue
+            body, _, comment = ln.partition("//")
+            vals = [int(v) for v in body.strip().strip("{},").split(",")]
+            N, K, M = vals[:3]
+            plan = dict(zip(keys, vals[3:]))
+            plan.update(vec_bytes=16, id=-1)
+            us = float(comment.split("us")[0]) if "us" in comment else 0.0
+            gbs = float(comment.split(",")[1].split("GB/s")[0]) if "GB/s" in comment else 0.0
+            out[(N, K, M)] = {"plan": plan, "us": us, "gbs": gbs}
+    return out
 
 
 def write_table(entries, path, note):
@@ -174,6 +196,8 @@ def main(argv=None):
     ap.add_argument("--min-bytes", type=float, default=float(1 << 30))
     ap.add_argument("--shapes", default=None, help="e.g. 4096x4096,2048x4096 (default: all)")
     ap.add_argument("--no-pair", action="store_true")
+    ap.add_argument("--merge", default=None,
+                    help="start from this existing table and replace only the swept entries")
     args = ap.parse_args(argv)
 
     assert torch.cuda.is_available(), "the sweep runs on the GPU"
@@ -188,7 +212,9 @@ def main(argv=None):
     if args.shapes:
         shapes = [tuple(int(v) for v in t.split("x")) for t in args.shapes.split(",")]
     t0 = time.time()
-    entries, dump = {}, {}
+    entries, dump = ({}, {})
+    if args.merge:
+        entries = read_table(args.merge)
     for (N, K) in shapes:
         res = sweep_shape(N, K, Ms, splits, flags, args.trials, args.replays, min_bytes)
         for M, r in res.items():
