@@ -27,7 +27,7 @@ __all__ = [
     "SGEMM_OK", "SGEMM_ERR_INVALID_ARG", "SGEMM_ERR_UNSUPPORTED_SHAPE", "SGEMM_ERR_MISALIGNED",
     "SGEMM_ERR_UNSUPPORTED_DEVICE", "SGEMM_ERR_NO_WORKSPACE", "SGEMM_ERR_CUDA", "MAX_BATCH",
     "SGEMM_VARIANT_LDG", "SGEMM_VARIANT_LDG_MIXFMA", "SGEMM_VARIANT_MMA", "SGEMM_VARIANT_MMA_T", "SGEMM_VARIANT_BULK", "SGEMM_VARIANT_LDG_FFMA2", "SGEMM_VARIANT_LDGX_MIXFMA",
-    "SGEMM_VARIANT_LDGX_FFMA2", "SGEMM_FLAG_PDL",
+    "SGEMM_VARIANT_LDGX_FFMA2", "SGEMM_VARIANT_MMA_TW", "SGEMM_VARIANT_LDG_MMA", "SGEMM_FLAG_PDL",
     "SGEMM_FLAG_TEST_STALL", "sgemm_device_errors",
     "SGEMM_FLAG_WEIGHTS_READONLY",
 ]
@@ -48,6 +48,8 @@ SGEMM_VARIANT_BULK = 4
 SGEMM_VARIANT_LDG_FFMA2 = 5
 SGEMM_VARIANT_LDGX_MIXFMA = 6
 SGEMM_VARIANT_LDGX_FFMA2 = 7
+SGEMM_VARIANT_MMA_TW = 8
+SGEMM_VARIANT_LDG_MMA = 9
 SGEMM_FLAG_TEST_STALL = 4
 SGEMM_FLAG_PDL = 1
 SGEMM_FLAG_WEIGHTS_READONLY = 2

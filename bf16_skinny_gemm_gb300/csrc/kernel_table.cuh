@@ -1,6 +1,7 @@
 // The compiled configurations of the weight-streaming kernel.  Each line is
 // (M, rows per lane group R, lanes per row LPR, loads per batch U, FMA mode
-// (0 widened, 1 mixed precision, 2 packed FP32x2), double-buffered batches);
+// (0 widened, 1 mixed precision, 2 packed FP32x2, 3 tensor cores on the diagonal of
+// mma.sync), double-buffered batches);
 // every configuration exists for M = 1..4.  The host
 // library enumerates these as plans (times two CTA sizes) and the offline
 // sweep times all of them.
@@ -10,6 +11,7 @@
 #include "skinny_mma.cuh"
 #include "skinny_mmat.cuh"
 #include "skinny_bulk.cuh"
+#include "skinny_mmatw.cuh"
 
 #define SK_LDG_CONFIGS(X, M)   \
     X(M, 1, 32, 8, 0, false)   \
@@ -32,7 +34,14 @@
     X(M, 2, 16, 2, 2, false)   \
     X(M, 1, 16, 4, 2, false)   \
     X(M, 4, 8, 2, 2, false)    \
-    X(M, 2, 32, 2, 2, true)
+    X(M, 2, 32, 2, 2, true)    \
+    X(M, 1, 32, 8, 3, false)   \
+    X(M, 2, 32, 4, 3, false)   \
+    X(M, 4, 32, 2, 3, false)   \
+    X(M, 2, 32, 2, 3, false)   \
+    X(M, 4, 32, 4, 3, false)   \
+    X(M, 1, 32, 4, 3, true)    \
+    X(M, 2, 32, 2, 3, true)
 
 // The same kernel reading x straight from global memory (no staging): (M, R,
 // LPR, U, FMA mode).
@@ -51,8 +60,9 @@
      reinterpret_cast<const void *>(&skinny_ldg_kernel<M, R, LPR, U, FMODE, false, true>)},
 
 #define SK_LDG_ENTRY(M, R, LPR, U, FMODE, DB)                                              \
-    {(FMODE) == 2 ? SGEMM_VARIANT_LDG_FFMA2                                               \
-                  : ((FMODE) == 1 ? SGEMM_VARIANT_LDG_MIXFMA : SGEMM_VARIANT_LDG),        \
+    {(FMODE) == 3   ? SGEMM_VARIANT_LDG_MMA                                               \
+     : (FMODE) == 2 ? SGEMM_VARIANT_LDG_FFMA2                                             \
+                    : ((FMODE) == 1 ? SGEMM_VARIANT_LDG_MIXFMA : SGEMM_VARIANT_LDG),      \
      M, R, LPR, U, (DB) ? 2 : 1,                                                          \
      reinterpret_cast<const void *>(&skinny_ldg_kernel<M, R, LPR, U, FMODE, DB>)},
 
@@ -69,6 +79,20 @@
 #define SK_MMA_ENTRY(M, U, DB)                          \
     {SGEMM_VARIANT_MMA, M, 16, 4, U, (DB) ? 2 : 1,      \
      reinterpret_cast<const void *>(&skinny_mma_kernel<M, U, DB>)},
+
+// Tensor-core kernel with x as the A operand and warp-owned 8-row tiles:
+// (M, k-blocks per batch U, double-buffered).  R = 8, LPR = 4.
+#define SK_MMATW_CONFIGS(X, M) \
+    X(M, 4, false)             \
+    X(M, 8, false)             \
+    X(M, 16, false)            \
+    X(M, 2, true)              \
+    X(M, 4, true)              \
+    X(M, 8, true)
+
+#define SK_MMATW_ENTRY(M, U, DB)                         \
+    {SGEMM_VARIANT_MMA_TW, M, 8, 4, U, (DB) ? 2 : 1,     \
+     reinterpret_cast<const void *>(&skinny_mmatw_kernel<M, U, DB>)},
 
 // Tensor-core configurations with x as the A operand: (M, U, double-buffered).
 // R = 8 rows per tile, 4 lanes share a row segment.
@@ -92,4 +116,5 @@
 #define SK_DEFINE_TABLE(M, NAME)                                                          \
     const KernelInfo NAME[] = {SK_LDG_CONFIGS(SK_LDG_ENTRY, M) SK_MMA_CONFIGS(SK_MMA_ENTRY, M) \
                                    SK_MMAT_CONFIGS(SK_MMAT_ENTRY, M) SK_BULK_ENTRY(M)     \
-                                       SK_LDGX_CONFIGS(SK_LDGX_ENTRY, M)};
+                                       SK_LDGX_CONFIGS(SK_LDGX_ENTRY, M)   \
+                                           SK_MMATW_CONFIGS(SK_MMATW_ENTRY, M)};

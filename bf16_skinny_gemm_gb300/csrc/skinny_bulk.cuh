@@ -35,15 +35,8 @@
 
 namespace sk {
 
-constexpr long long kWaitLimitNs = 200LL * 1000 * 1000;  // 0.2 s per wait
-
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
 }
 __device__ __forceinline__ void mbar_init(uint64_t *b, unsigned count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");

@@ -63,6 +63,16 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // Returns at once when the kernel was not launched as a programmatic dependent.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Every wait of a kernel on something outside its own CTA is bounded on the
+// global nanosecond timer; a wait that runs out reports it in the device error
+// word instead of hanging the GPU.
+constexpr long long kWaitLimitNs = 200LL * 1000 * 1000;  // 0.2 s per wait
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
 // BF16 -> FP32 is exact: the BF16 bits are the top half of the FP32 bits.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -84,6 +94,16 @@ __device__ __forceinline__ float fma2_bf16(uint32_t xw, uint32_t ww, float acc) 
     return acc;
 }
 
+// D[16x8] += A[16x16] . B[16x8], BF16 inputs, FP32 accumulation (mma.sync).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // 16 bytes of x: from shared memory (staged), or straight from global memory
 // through the L1 cache (x is a few KiB and stays there after the first touch).
 template <bool XG>
@@ -99,8 +119,18 @@ __device__ __forceinline__ uint4 load_x(const uint4 *p) {
 //   2: packed FP32x2 FMA (fma.rn.f32x2, sm_100+): each accumulator is a pair
 //      {even k, odd k} of FP32 partial sums, one instruction per two elements;
 //      the pair is added (even + odd) when the row is finished.
-// Modes 0 and 1 round identically (one rounding per element); mode 2 keeps two
-// partial sums and so a different, equally fixed, summation order.
+//   3: the tensor core on the same data layout (LPR = 32, so lane l holds
+//      k = 8l .. 8l+7 of each 256-element chunk of a row): in one mma.sync
+//      m16n8k16 the 8 columns of B are the chunk's 8 segments of 32 elements
+//      (lanes 4g .. 4g+3 hold segment g, each lane its own 16 bytes, the
+//      first 8 bytes in one MMA and the last 8 in a second), and row g (g+8)
+//      of A is x row m (m+1) at the k of segment g -- which are exactly the k
+//      of the lane's own x chunk.  So D[g][g] (D[g+8][g]) accumulates x_m
+//      (x_{m+1}) . W over segment g; the off-diagonal entries are not used.
+//      Two MMAs per 16 bytes of W and pair of x rows instead of 8 FMAs per x
+//      row; the 8 diagonal entries are added by the butterfly at row end.
+// Modes 0 and 1 round identically (one rounding per element); modes 2 and 3
+// each keep their own, equally fixed, summation order.
 template <int M, int FMODE>
 struct XChunk;
 
@@ -207,9 +237,55 @@ struct XChunk<M, 2> {
     }
 };
 
+template <int M>
+struct XChunk<M, 3> {
+    struct Acc {
+        float d[4];  // D fragment of the x-row pair (m, m+1), kept at even m
+    };
+    uint32_t v[M][4];
+    // this lane's share of row m's sum: its diagonal entry of D, if it holds one
+    template <int R>
+    static __device__ __forceinline__ float diag(const Acc (&acc)[M][R], int m, int r) {
+        const int lane = threadIdx.x & 31;
+        const int g = lane >> 2, c = lane & 3;
+        if (c != (g >> 1)) return 0.0f;  // D[g][g] sits in lane (g, g/2), element g%2
+        const Acc &a = acc[m & ~1][r];
+        return (m & 1) ? ((g & 1) ? a.d[3] : a.d[2]) : ((g & 1) ? a.d[1] : a.d[0]);
+    }
+    template <bool XG>
+    __device__ __forceinline__ void load(const uint4 *xs, long long stride, int c) {
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            const uint4 q = load_x<XG>(xs + m * stride + c);
+            v[m][0] = q.x;
+            v[m][1] = q.y;
+            v[m][2] = q.z;
+            v[m][3] = q.w;
+        }
+    }
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int m = 0; m < M; ++m) v[m][0] = v[m][1] = v[m][2] = v[m][3] = 0u;
+    }
+    // called by all 32 lanes together (mma.sync), never under a lane-dependent branch
+    template <int R>
+    __device__ __forceinline__ void fma(Acc (&acc)[M][R], const uint4 &w, int r) const {
+#pragma unroll
+        for (int m = 0; m < M; m += 2) {
+            const uint32_t y0 = m + 1 < M ? v[m + 1][0] : 0u, y1 = m + 1 < M ? v[m + 1][1] : 0u;
+            const uint32_t y2 = m + 1 < M ? v[m + 1][2] : 0u, y3 = m + 1 < M ? v[m + 1][3] : 0u;
+            const uint32_t a0[4] = {v[m][0], y0, v[m][1], y1};
+            const uint32_t a1[4] = {v[m][2], y2, v[m][3], y3};
+            mma_bf16_16816(acc[m][r].d, a0, w.x, w.y);
+            mma_bf16_16816(acc[m][r].d, a1, w.z, w.w);
+        }
+    }
+};
+
 template <int M, int R, int LPR, int U, int FMODE, bool DB, bool XG = false>
 __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_constant__ Params p) {
     static_assert(LPR == 32 || LPR == 16 || LPR == 8, "lanes per row");
+    static_assert(FMODE != 3 || LPR == 32, "the tensor-core mode spreads a row over the warp");
     constexpr int G = 32 / LPR;  // lane groups per warp
     extern __shared__ uint4 xs[];  // [M][nchunk] chunks of 8 BF16
 
@@ -296,14 +372,26 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
 #pragma unroll
     for (int m = 0; m < M; ++m)
 #pragma unroll
-        for (int r = 0; r < R; ++r) acc[m][r] = Acc(0);
+        for (int r = 0; r < R; ++r) acc[m][r] = Acc{};
 
     int ct = 0, cj = 0;
     auto consume_batch = [&](const Batch &buf, int base) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (base + u < total) {
-                if ((cj < jtot - 1) || (li < last_lanes)) {
+                const bool active = (cj < jtot - 1) || (li < last_lanes);
+                if constexpr (FMODE == 3) {
+                    // mma.sync is a warp-wide instruction: every lane takes part, and
+                    // the lanes past the end of the row bring zero x (their W is zero)
+                    XC xc;
+                    if (active) {
+                        xc.template load<XG>(xsrc, xstride, li + LPR * cj);
+                    } else {
+                        xc.zero();
+                    }
+#pragma unroll
+                    for (int r = 0; r < R; ++r) xc.template fma<R>(acc, buf[u][r], r);
+                } else if (active) {
                     XC xc;
                     xc.template load<XG>(xsrc, xstride, li + LPR * cj);
 #pragma unroll
@@ -316,7 +404,12 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
                     for (int m = 0; m < M; ++m)
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
-                            float v = XC::total(acc[m][r]);
+                            float v;
+                            if constexpr (FMODE == 3) {
+                                v = XC::diag(acc, m, r);
+                            } else {
+                                v = XC::total(acc[m][r]);
+                            }
 #pragma unroll
                             for (int off = LPR / 2; off >= 1; off >>= 1)
                                 v += __shfl_xor_sync(0xffffffffu, v, off);
@@ -344,7 +437,7 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
 #pragma unroll
                     for (int m = 0; m < M; ++m)
 #pragma unroll
-                        for (int r = 0; r < R; ++r) acc[m][r] = Acc(0);
+                        for (int r = 0; r < R; ++r) acc[m][r] = Acc{};
                     cj = 0;
                     ++ct;
                 }

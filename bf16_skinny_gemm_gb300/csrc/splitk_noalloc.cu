@@ -13,8 +13,11 @@
 //
 // The kernels are the regular ones of the selected plan (the streaming kernel
 // with gridDim.y splits, then splitk_reduce_kernel; a CUDA-core plan when the
-// selected one cannot split K); only where the FP32 partial sums live differs,
-// so results are bitwise equal to sgemm_bf16_skinny_ex with that plan.
+// selected one is the bulk-copy kernel, which cannot split K, and the x-as-A
+// tensor-core kernel with CTA-wide tiles when the selected one is its
+// warp-owned-tile form, whose split_k splits K inside a CTA); only where the
+// FP32 partial sums live differs, so results are bitwise equal to
+// sgemm_bf16_skinny_ex with that plan.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -120,6 +123,10 @@ extern "C" sgemm_status_t sgemm_bf16_skinny_splitk_noalloc(
         plan.lanes_per_row = 32;
         plan.k_unroll = 8;
         plan.stages = 1;
+        plan.ctas_per_sm = 0;
+    }
+    if (plan.variant == SGEMM_VARIANT_MMA_TW) {
+        plan.variant = SGEMM_VARIANT_MMA_T;
         plan.ctas_per_sm = 0;
     }
     sgemm_status_t s = sgemm_plan_check(&plan, M, N, K);

@@ -47,6 +47,9 @@ DEFAULT_OUT = os.path.join(HERE, "csrc", "plan_table.inc")
 
 # bulk-copy kernel geometry: (stage width in 32-element k-blocks, ring slots)
 BULK_GEOMETRY = [(16, 8), (32, 4), (32, 6), (64, 2), (64, 3)]
+# warp-owned-tile tensor-core kernel: warps sharing a tile's K range x CTAs per SM
+TW_SPLITS = [1, 2, 4, 8]
+TW_CTAS = [0, 1, 2]
 
 
 def candidates(M, N, K, splits):
@@ -55,6 +58,8 @@ def candidates(M, N, K, splits):
         base = sk.sgemm_plan_get(i)
         if base.variant == sk.SGEMM_VARIANT_BULK:
             variants = [base.copy(k_unroll=kb, stages=ring) for kb, ring in BULK_GEOMETRY]
+        elif base.variant == sk.SGEMM_VARIANT_MMA_TW:
+            variants = [base.copy(split_k=s, ctas_per_sm=c) for s in TW_SPLITS for c in TW_CTAS]
         else:
             variants = [base.copy(split_k=s) for s in splits]
         for p in variants:

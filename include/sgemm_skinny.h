@@ -114,7 +114,23 @@ enum {
     SGEMM_VARIANT_LDGX_MIXFMA = 6, /* variant 1 reading x from global memory through L1 at each
                                      use instead of staging it in shared memory (no CTA barrier
                                      before the first FMA); same results as variants 0/1 */
-    SGEMM_VARIANT_LDGX_FFMA2 = 7  /* variant 5 with x read the same way; same results as 5 */
+    SGEMM_VARIANT_LDGX_FFMA2 = 7, /* variant 5 with x read the same way; same results as 5 */
+    SGEMM_VARIANT_MMA_TW = 8,     /* the tensor-core math of variant 3 (x as A, 8-row tiles)
+                                     with warp-owned tiles: each warp streams its tiles' rows
+                                     along K on its own, with no CTA barrier after x is staged,
+                                     and writes y from its MMA fragment.  split_k here is the
+                                     number of warps of a CTA that share each tile's K range (1,
+                                     2, 4 or 8, dividing threads/32 and at most the 32-element
+                                     k-blocks of a row); they add their fragments in shared
+                                     memory, in order, with no second pass and no scratch.
+                                     rows_per_warp = 8, lanes_per_row = 4 */
+    SGEMM_VARIANT_LDG_MMA = 9     /* the streaming kernel of variant 1 (one row's 512 bytes per
+                                     load instruction, lanes_per_row = 32) with the products
+                                     done by mma.sync m16n8k16: the 8 columns of B are the 8
+                                     consecutive 32-element segments a warp load covers, A holds
+                                     x rows m and m+1 at the same k, and the diagonal of D is the
+                                     per-segment dot product (2 MMAs per 16 bytes of W and pair
+                                     of x rows, instead of 8 FMAs per x row) */
 };
 
 /* Launch flags (bit set) for the _ex calls.
