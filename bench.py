@@ -110,8 +110,8 @@ def measured_peaks():
 
 # The streaming kernels' sources, their compiled configurations, the plan table and
 # the launch geometry: what the recorded DRAM traffic per launch depends on.
-KERNEL_SOURCES = ["skinny_ldg.cuh", "skinny_mma.cuh", "kernel_table.cuh", "internal.h",
-                  "plan_table.inc", "api.cpp"]
+KERNEL_SOURCES = ["skinny_ldg.cuh", "skinny_mma.cuh", "skinny_mmat.cuh", "skinny_mmatw.cuh",
+                  "skinny_bulk.cuh", "kernel_table.cuh", "internal.h", "plan_table.inc", "api.cpp"]
 
 
 def kernel_source_hash():
