@@ -19,7 +19,9 @@ Reported (one JSON line on rank 0):
 - cpu_baseline: the CPU oracle timed on a bounded sample on this host.
 
 ``--impl reference`` times the CPU oracle alone (the reference arm).
-``--workload`` selects other configurations: single, lmhead, pairs, chain.
+``--workload`` selects other configurations: single, lmhead, pairs, chain (with
+the elementwise step separate and fused into the GEMM epilogue), router (the
+FP32-output router gate).
 """
 from __future__ import annotations
 
@@ -43,6 +45,7 @@ SWEEP_SHAPES = [(12576, 4096), (4096, 4096), (2048, 4096), (4096, 1024), (8192, 
 SWEEP_MS = [1, 2, 4]
 LMHEAD = (77440, 4096)
 PAIR = (4096, 128)
+ROUTER = (288, 4096)
 CHAIN = [((12576, 4096), 34), ((4096, 4096), 34), ((2048, 4096), 53), ((4096, 1024), 42),
          ((8192, 1536), 11), ((4096, 8192), 11), ((77440, 4096), 1)]
 FALLBACK_HBM_GBS = 6800.0
@@ -534,12 +537,27 @@ def run_chain(args, torch, sk, synth, dist):
         for i in range(len(seq) - 1):
             sk.sgemm_bf16_rescale(ys[i], xs[i + 1], scales[i], flags=flags & sk.SGEMM_FLAG_PDL)
 
+    def fused_step():
+        # the elementwise step in each GEMM's epilogue: 186 launches instead of 371
+        for i in range(len(seq)):
+            if i + 1 < len(seq):
+                sk.sgemm_bf16_skinny_rescale_ex(xs[i], Ws[i], ys[i], xs[i + 1], scales[i],
+                                                flags=flags)
+            else:
+                sk.sgemm_bf16_skinny_ex(xs[i], Ws[i], ys[i], flags=flags)
+
     step()
     torch.cuda.synchronize()
+    y_last = ys[-1].clone()
+    fused_step()
+    torch.cuda.synchronize()
+    if not torch.equal(ys[-1].view(torch.int16), y_last.view(torch.int16)):
+        raise SystemExit("fused chain step differs from the separate one")
     g_step = _capture(torch, step)
     g_elt = _capture(torch, elementwise_only)
-    per, total_s = _time_graphs(torch, dist, [g_step, g_elt], args.steps, args.warmup)
-    step_ms, elt_ms = per
+    g_fused = _capture(torch, fused_step)
+    per, total_s = _time_graphs(torch, dist, [g_step, g_elt, g_fused], args.steps, args.warmup)
+    step_ms, elt_ms, fused_ms = per
     w_bytes = sum(2 * N * K for (N, K) in seq)
     alg = sum(gemm_bytes(1, N, K) for (N, K) in seq)
     gemm_ms = step_ms - elt_ms
@@ -559,8 +577,14 @@ def run_chain(args, torch, sk, synth, dist):
                       "gemm_us": round(gemm_ms * 1e3, 1),
                       "gemm_us_at_measured_peak": round(alg / (peak * 1e9) * 1e6, 1),
                       "frac_of_peak": round(alg / (gemm_ms / 1e3) / 1e9 / peak, 4),
-                      "peak_source": src},
-            "gpu_launches": (2 * len(seq) - 1) * args.steps}
+                      "peak_source": src,
+                      "fused_step_us": round(fused_ms * 1e3, 1),
+                      "fused_gbs": round(alg / (fused_ms / 1e3) / 1e9, 1),
+                      "fused_frac_of_peak": round(alg / (fused_ms / 1e3) / 1e9 / peak, 4),
+                      "fused_note": "the same chain with the elementwise step in each GEMM's "
+                                    "epilogue (sgemm_bf16_skinny_rescale_ex), whole step, "
+                                    "nothing subtracted; outputs bitwise equal"},
+            "gpu_launches": ((2 * len(seq) - 1) + (len(seq) - 1) + len(seq)) * args.steps}
     if rank == 0:
         print(json.dumps(line), flush=True)
         if args.detail_out:
@@ -585,13 +609,76 @@ def sweep_config_desc(gs):
     return d
 
 
+def run_router(args, torch, sk, synth, dist, min_bytes):
+    """The MoE router gate (N, K) = (288, 4096) with FP32 outputs, M = 1..4, the
+    projection vLLM PR #62949 (Validation, the nsys census) leaves on cuBLAS for
+    its FP32 output.  Each M: a CUDA graph of R GEMMs on R weight copies (cold),
+    FP32 outputs (sgemm_bf16_skinny_f32out_ex) and, for comparison, BF16 outputs."""
+    ws, rank, _ = dist_info()
+    N, K = ROUTER
+    dev = torch.device("cuda")
+    R = max(2, math.ceil(min_bytes / (2 * N * K)))
+    W = torch.empty((R, N, K), dtype=torch.bfloat16, device=dev)
+    for i in range(R):
+        W[i].copy_(synth.normal_bf16((N, K), synth.W_STD, seed=i, device=dev))
+    flags = sk.SGEMM_FLAG_PDL | sk.SGEMM_FLAG_WEIGHTS_READONLY
+    detail, graphs, keep, nbytes = [], [], [], 0
+    for M in [1, 2, 3, 4]:
+        x = synth.normal_bf16((R, M, K), synth.X_STD, seed=200 + M, device=dev)
+        y32 = torch.empty((R, M, N), dtype=torch.float32, device=dev)
+        y16 = torch.empty((R, M, N), dtype=torch.bfloat16, device=dev)
+        keep.append((x, y32, y16))
+
+        def f32():
+            for i in range(R):
+                sk.sgemm_bf16_skinny_f32out_ex(x[i], W[i], y32[i], flags=flags)
+
+        def b16():
+            for i in range(R):
+                sk.sgemm_bf16_skinny_ex(x[i], W[i], y16[i], flags=flags)
+
+        f32()
+        b16()
+        torch.cuda.synchronize()
+        graphs += [_capture(torch, f32), _capture(torch, b16)]
+        detail.append({"M": M, "copies": R})
+        nbytes += R * (2 * (N * K + M * K) + 4 * M * N)
+    per, _ = _time_graphs(torch, dist, graphs, args.steps, args.warmup)
+    del graphs, keep
+    total_ms = 0.0
+    for d, (f_ms, b_ms) in zip(detail, zip(per[0::2], per[1::2])):
+        d["us_f32_out"] = round(f_ms * 1e3 / d["copies"], 3)
+        d["us_bf16_out"] = round(b_ms * 1e3 / d["copies"], 3)
+        d["gbs_f32_out"] = round((2 * (N * K + d["M"] * K) + 4 * d["M"] * N)
+                                 / (f_ms * 1e3 / d["copies"]) / 1e3, 1)
+        total_ms += f_ms
+    value = dist.sum(nbytes) / (dist.max(total_ms) / 1e3) / 1e9
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "router gate (N,K)=(288,4096), FP32 outputs, M=1..4",
+                       "x": "BF16 ~ N(0,1)", "W": "BF16 ~ N(0,0.02^2)",
+                       "l2": "inputs larger than L2 (rotating weight copies)",
+                       "launch_flags": "pdl,readonly", "parallelism": "replicas"},
+            "gpu_launches": sum(d["copies"] * 2 for d in detail) * args.steps,
+            "detail": detail}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+        if args.detail_out:
+            with open(args.detail_out, "w") as f:
+                json.dump(line, f, indent=1)
+    dist.close()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["sweep", "single", "lmhead", "pairs", "chain"],
+    ap.add_argument("--workload", choices=["sweep", "single", "lmhead", "pairs", "chain", "router"],
                     default="sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -642,6 +729,8 @@ def main():
         cases = [(LMHEAD[0], LMHEAD[1], M) for M in SWEEP_MS]
     elif args.workload == "pairs":
         return run_pairs(args, torch, sk, synth, dist, min_bytes)
+    elif args.workload == "router":
+        return run_router(args, torch, sk, synth, dist, min_bytes)
     else:
         return run_chain(args, torch, sk, synth, dist)
 

@@ -24,6 +24,7 @@ __all__ = [
     "sgemm_bf16_skinny_batched_ex", "sgemm_plan_select", "sgemm_plan_count", "sgemm_plan_get",
     "sgemm_plan_check", "sgemm_init", "sgemm_status_string", "sgemm_version",
     "sgemm_bf16_skinny_splitk_noalloc", "NOALLOC_SCRATCH_BYTES", "sgemm_bf16_rescale",
+    "sgemm_bf16_skinny_rescale_ex", "sgemm_bf16_skinny_f32out_ex",
     "SGEMM_OK", "SGEMM_ERR_INVALID_ARG", "SGEMM_ERR_UNSUPPORTED_SHAPE", "SGEMM_ERR_MISALIGNED",
     "SGEMM_ERR_UNSUPPORTED_DEVICE", "SGEMM_ERR_NO_WORKSPACE", "SGEMM_ERR_CUDA", "MAX_BATCH",
     "SGEMM_VARIANT_LDG", "SGEMM_VARIANT_LDG_MIXFMA", "SGEMM_VARIANT_MMA", "SGEMM_VARIANT_MMA_T", "SGEMM_VARIANT_BULK", "SGEMM_VARIANT_LDG_FFMA2", "SGEMM_VARIANT_LDGX_MIXFMA",
@@ -114,6 +115,12 @@ def load() -> ctypes.CDLL:
         lib.sgemm_bf16_skinny_ex.argtypes = [vp, ll, vp, vp, ll, ci, ci, ci,
                                              ctypes.POINTER(Plan), cu, vp]
         lib.sgemm_bf16_skinny_ex.restype = ci
+        lib.sgemm_bf16_skinny_rescale_ex.argtypes = [vp, ll, vp, vp, ll, ci, ci, ci, vp, ll, ll,
+                                                     ctypes.c_float, ctypes.POINTER(Plan), cu, vp]
+        lib.sgemm_bf16_skinny_rescale_ex.restype = ci
+        lib.sgemm_bf16_skinny_f32out_ex.argtypes = [vp, ll, vp, vp, ll, ci, ci, ci,
+                                                    ctypes.POINTER(Plan), cu, vp]
+        lib.sgemm_bf16_skinny_f32out_ex.restype = ci
         lib.sgemm_bf16_skinny_batched.argtypes = [ctypes.POINTER(Pair), ci, ci, ci, ci, vp]
         lib.sgemm_bf16_skinny_batched.restype = ci
         lib.sgemm_bf16_skinny_batched_ex.argtypes = [ctypes.POINTER(Pair), ci, ci, ci, ci,
@@ -201,6 +208,50 @@ def sgemm_bf16_skinny_ex(x: torch.Tensor, W: torch.Tensor, y: torch.Tensor | Non
     _check(load().sgemm_bf16_skinny_ex(x.data_ptr(), ldx, W.data_ptr(), y.data_ptr(), ldy,
                                        M, N, K, ctypes.byref(plan) if plan is not None else None,
                                        int(flags), _stream(stream)), "sgemm_bf16_skinny_ex")
+    return y
+
+
+def sgemm_bf16_skinny_rescale_ex(x: torch.Tensor, W: torch.Tensor, y: torch.Tensor,
+                                 x_next: torch.Tensor, scale: float, plan: Plan | None = None,
+                                 flags: int = 0, stream=None) -> torch.Tensor:
+    """One decode-chain GEMM with the elementwise step fused into its epilogue:
+    ``y = x @ W.T`` and ``x_next[m, k] = bf16(float(y[m, k % N]) * scale)`` for every
+    column k of x_next ([M, n_next] BF16, its own buffer).  Returns y."""
+    M, N, K, y = _problem(x, W, y)
+    _bf16_2d(x_next, "x_next")
+    if x_next.shape[0] != M:
+        raise ValueError(f"x_next must have {M} rows, got {x_next.shape[0]}")
+    n_next = x_next.shape[1]
+    ldx = x.stride(0) if M > 1 else K
+    ldy = y.stride(0) if M > 1 else N
+    ldn = x_next.stride(0) if M > 1 else n_next
+    _check(load().sgemm_bf16_skinny_rescale_ex(
+        x.data_ptr(), ldx, W.data_ptr(), y.data_ptr(), ldy, M, N, K, x_next.data_ptr(), ldn,
+        n_next, float(scale), ctypes.byref(plan) if plan is not None else None, int(flags),
+        _stream(stream)), "sgemm_bf16_skinny_rescale_ex")
+    return y
+
+
+def sgemm_bf16_skinny_f32out_ex(x: torch.Tensor, W: torch.Tensor, y: torch.Tensor | None = None,
+                                plan: Plan | None = None, flags: int = 0,
+                                stream=None) -> torch.Tensor:
+    """``y = x @ W.T`` with FP32 outputs (y: float32 [M, N], row-strided allowed)."""
+    _bf16_2d(x, "x")
+    _bf16_2d(W, "W")
+    M, K = x.shape
+    N = W.shape[0]
+    if W.shape[1] != K or (W.stride(0) != K and N > 1):
+        raise ValueError(f"W must be a contiguous [N, {K}] tensor, got {tuple(W.shape)}")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    if y.dtype != torch.float32 or y.dim() != 2 or tuple(y.shape) != (M, N) or y.stride(1) != 1:
+        raise ValueError(f"y must be a float32 [{M}, {N}] tensor with unit column stride")
+    ldx = x.stride(0) if M > 1 else K
+    ldy = y.stride(0) if M > 1 else N
+    _check(load().sgemm_bf16_skinny_f32out_ex(
+        x.data_ptr(), ldx, W.data_ptr(), y.data_ptr(), ldy, M, N, K,
+        ctypes.byref(plan) if plan is not None else None, int(flags), _stream(stream)),
+        "sgemm_bf16_skinny_f32out_ex")
     return y
 
 

@@ -246,8 +246,40 @@ sgemm_status_t validate_item(const sgemm_pair_t &it, int N, int K) {
     return SGEMM_OK;
 }
 
+// What the kernels' epilogue writes besides BF16 y (see store_out in skinny_ldg.cuh).
+struct Epilogue {
+    bool out_f32 = false;     // y is FP32
+    uint16_t *xn = nullptr;   // fused chain step: the next GEMM's input (single problem only)
+    long long ldxn = 0;
+    long long xn_len = 0;
+    float xn_scale = 1.0f;
+};
+
+// Byte ranges [a, a + na) and [b, b + nb) overlap.
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+sgemm_status_t validate_epilogue(const Epilogue &ep, const sgemm_pair_t &it, int M, int N, int K) {
+    if (ep.out_f32 && (reinterpret_cast<uintptr_t>(it.y) & 3u)) return SGEMM_ERR_MISALIGNED;
+    if (!ep.xn) return SGEMM_OK;
+    if (ep.xn_len < 1 || ep.xn_len > 0x7fffffffLL || ep.ldxn < ep.xn_len) return SGEMM_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(ep.xn) & 1u) return SGEMM_ERR_MISALIGNED;
+    // the next input is written while this GEMM still reads x and W and writes y
+    const size_t xn_bytes = (static_cast<size_t>(M - 1) * ep.ldxn + ep.xn_len) * 2;
+    const size_t x_bytes = (static_cast<size_t>(M - 1) * it.ldx + K) * 2;
+    const size_t y_bytes = (static_cast<size_t>(M - 1) * it.ldy + N) * 2;
+    const size_t w_bytes = static_cast<size_t>(N) * K * 2;
+    if (overlaps(ep.xn, xn_bytes, it.x, x_bytes) || overlaps(ep.xn, xn_bytes, it.y, y_bytes) ||
+        overlaps(ep.xn, xn_bytes, it.W, w_bytes))
+        return SGEMM_ERR_INVALID_ARG;
+    return SGEMM_OK;
+}
+
 sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
-                   const sgemm_plan_t *plan_in, unsigned flags, cudaStream_t stream) {
+                   const sgemm_plan_t *plan_in, unsigned flags, cudaStream_t stream,
+                   const Epilogue &ep = Epilogue()) {
     sgemm_status_t s = validate_common(M, N, K, batch);
     if (s != SGEMM_OK) return s;
     if (flags & ~(SGEMM_FLAG_PDL | SGEMM_FLAG_WEIGHTS_READONLY | SGEMM_FLAG_TEST_STALL))
@@ -256,7 +288,10 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
     for (int b = 0; b < batch; ++b) {
         s = validate_item(items[b], N, K);
         if (s != SGEMM_OK) return s;
+        s = validate_epilogue(ep, items[b], M, N, K);
+        if (s != SGEMM_OK) return s;
     }
+    if (ep.xn && batch != 1) return SGEMM_ERR_INVALID_ARG;
     const sgemm_plan_t plan = plan_in ? *plan_in : sgemm_plan_select(N, K, M);
     s = check_plan(plan, M, N, K);
     if (s != SGEMM_OK) return s;
@@ -282,7 +317,12 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
         prm.item[b].y = items[b].y;
         prm.item[b].ldx = items[b].ldx;
         prm.item[b].ldy = items[b].ldy;
+        prm.item[b].xn = ep.xn;
+        prm.item[b].ldxn = ep.ldxn;
     }
+    prm.out_f32 = ep.out_f32 ? 1 : 0;
+    prm.xn_len = static_cast<int>(ep.xn_len);
+    prm.xn_scale = ep.xn_scale;
     prm.N = N;
     prm.K = K;
     prm.kps = kps;
@@ -474,6 +514,42 @@ sgemm_status_t sgemm_bf16_skinny_ex(const sgemm_bf16_t *x, long long ldx, const 
     it.ldx = ldx;
     it.ldy = ldy;
     return run(&it, 1, M, N, K, plan, flags, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sgemm_status_t sgemm_bf16_skinny_f32out_ex(const sgemm_bf16_t *x, long long ldx,
+                                           const sgemm_bf16_t *W, float *y, long long ldy, int M,
+                                           int N, int K, const sgemm_plan_t *plan, unsigned flags,
+                                           sgemm_stream_t stream) {
+    sgemm_pair_t it;
+    it.x = x;
+    it.W = W;
+    it.y = reinterpret_cast<sgemm_bf16_t *>(y);
+    it.ldx = ldx;
+    it.ldy = ldy;
+    Epilogue ep;
+    ep.out_f32 = true;
+    return run(&it, 1, M, N, K, plan, flags, reinterpret_cast<cudaStream_t>(stream), ep);
+}
+
+sgemm_status_t sgemm_bf16_skinny_rescale_ex(const sgemm_bf16_t *x, long long ldx,
+                                            const sgemm_bf16_t *W, sgemm_bf16_t *y, long long ldy,
+                                            int M, int N, int K, sgemm_bf16_t *x_next,
+                                            long long ld_next, long long n_next, float scale,
+                                            const sgemm_plan_t *plan, unsigned flags,
+                                            sgemm_stream_t stream) {
+    if (!x_next) return SGEMM_ERR_INVALID_ARG;
+    sgemm_pair_t it;
+    it.x = x;
+    it.W = W;
+    it.y = y;
+    it.ldx = ldx;
+    it.ldy = ldy;
+    Epilogue ep;
+    ep.xn = x_next;
+    ep.ldxn = ld_next;
+    ep.xn_len = n_next;
+    ep.xn_scale = scale;
+    return run(&it, 1, M, N, K, plan, flags, reinterpret_cast<cudaStream_t>(stream), ep);
 }
 
 sgemm_status_t sgemm_bf16_skinny(const sgemm_bf16_t *x, const sgemm_bf16_t *W, sgemm_bf16_t *y,

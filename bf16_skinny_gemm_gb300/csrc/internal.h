@@ -21,9 +21,11 @@ constexpr size_t kMaxSmemOptin = 227 * 1024;  // shared memory a CTA may opt in 
 struct Item {
     const uint16_t *x;
     const uint16_t *W;
-    uint16_t *y;
+    uint16_t *y;       // BF16 outputs, or FP32 outputs (reinterpreted) when Params::out_f32
     long long ldx;
     long long ldy;
+    uint16_t *xn;      // fused chain epilogue: the next GEMM's input, or null
+    long long ldxn;
 };
 
 // Params::flags bits (the launch flags of the C ABI, SGEMM_FLAG_*).
@@ -43,6 +45,9 @@ struct Params {
     int flags;       // SGEMM_FLAG_* bits
     int ring;        // bulk-copy kernel: shared-memory ring slots
     int *err;        // bulk-copy kernel: device error word (bit 0: a wait gave up); may be null
+    int out_f32;     // 1: y holds FP32 outputs (no BF16 rounding)
+    int xn_len;      // fused chain epilogue: xn[m][k] for 0 <= k < xn_len ...
+    float xn_scale;  // ... = RNE_bf16(float(y[m][k mod N]) * xn_scale)
 };
 
 #ifdef __CUDACC__

@@ -81,6 +81,26 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
+// The epilogue of every kernel: output (m, n) of problem `it`, FP32 sum v.
+//  - BF16 output: y = RNE_bf16(v).  With the fused chain epilogue, the next
+//    GEMM's input also gets xn[m][k] = RNE_bf16(float(y) * scale) for every
+//    k < xn_len with k = n (mod N): the elementwise step between the decode
+//    chain's GEMMs, done on the value just rounded, so the result is bitwise
+//    that of the separate step.
+//  - FP32 output: y = v, no rounding.
+__device__ __forceinline__ void store_out(const Params &p, const Item &it, int m, int n, float v) {
+    if (p.out_f32) {
+        reinterpret_cast<float *>(it.y)[m * it.ldy + n] = v;
+        return;
+    }
+    const uint16_t b = f32_to_bf16_rn(v);
+    it.y[m * it.ldy + n] = b;
+    if (it.xn) {
+        const uint16_t q = f32_to_bf16_rn(__uint_as_float(static_cast<uint32_t>(b) << 16) * p.xn_scale);
+        for (int k = n; k < p.xn_len; k += p.N) it.xn[m * it.ldxn + k] = q;
+    }
+}
+
 // acc += lo(x)*lo(w), then acc += hi(x)*hi(w): BF16 operands, FP32 addend,
 // one round-to-nearest per FMA.
 __device__ __forceinline__ float fma2_bf16(uint32_t xw, uint32_t ww, float acc) {
@@ -424,7 +444,7 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
 #pragma unroll
                                 for (int m = 0; m < M; ++m) {
                                     if (p.split == 1) {
-                                        it.y[m * it.ldy + n] = f32_to_bf16_rn(tot[m][r]);
+                                        store_out(p, it, m, n, tot[m][r]);
                                     } else {
                                         const long long slot =
                                             (static_cast<long long>(blockIdx.z) * p.split + s) * M + m;
@@ -484,7 +504,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
         float acc = 0.0f;
         for (int s = 0; s < p.split; ++s) acc += src[static_cast<long long>(s) * M * p.N];
         const Item &it = p.item[b];
-        it.y[m * it.ldy + n] = f32_to_bf16_rn(acc);
+        store_out(p, it, m, n, acc);
     }
 }
 

@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mma_kernel(const __grid_co
                         for (int w = 0; w < NW; ++w) v += rr[w * TILE * 4];
                         if (n < p.N) {
                             if (p.split == 1) {
-                                it.y[m * it.ldy + n] = f32_to_bf16_rn(v);
+                                store_out(p, it, m, n, v);
                             } else {
                                 const long long slot =
                                     (static_cast<long long>(blockIdx.z) * p.split + s) * M + m;

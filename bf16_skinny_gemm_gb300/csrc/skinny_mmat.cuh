@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mmat_kernel(const __grid_c
                         for (int ww = 0; ww < NW; ++ww) v += rr[ww * TILE * M];
                         if (n < p.N) {
                             if (p.split == 1) {
-                                it.y[m * it.ldy + n] = f32_to_bf16_rn(v);
+                                store_out(p, it, m, n, v);
                             } else {
                                 const long long slot =
                                     (static_cast<long long>(blockIdx.z) * p.split + s) * M + m;

@@ -140,8 +140,8 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mmatw_kernel(const __grid_
                     }
                     if (write && g < M) {
                         const int n = ct * TILE + 2 * c;
-                        if (n < p.N) it.y[g * it.ldy + n] = f32_to_bf16_rn(v0);
-                        if (n + 1 < p.N) it.y[g * it.ldy + n + 1] = f32_to_bf16_rn(v1);
+                        if (n < p.N) store_out(p, it, g, n, v0);
+                        if (n + 1 < p.N) store_out(p, it, g, n + 1, v1);
                     }
                     acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
                     ci = 0;

@@ -221,12 +221,44 @@ sgemm_status_t sgemm_plan_check(const sgemm_plan_t *plan, int M, int N, int K);
  * streams must be ordered by the caller. */
 sgemm_status_t sgemm_init(void);
 
-/* The elementwise step between consecutive GEMMs of a decode chain ("a small
- * kernel between GEMMs", vLLM PR #65306, Validation):
+/* The elementwise step between consecutive GEMMs of a decode chain (vLLM PR
+ * #65306, Validation: the chain's GEMMs are separated by a short elementwise
+ * kernel):
  *     x[k] = RNE_bf16( float(y[k mod n_src]) * scale )   for 0 <= k < n_dst.
  * y and x are DEVICE arrays of BF16 bits (2-byte aligned, not overlapping).
  * flags: SGEMM_FLAG_PDL launches it as a programmatic dependent (it waits for
  * the previous kernel before reading y).  Errors as for the GEMM calls. */
+/* One GEMM of a decode chain with that elementwise step fused into its
+ * epilogue: y = x . W^T as sgemm_bf16_skinny_ex (same plan, same bits), and
+ *     x_next[m][k] = RNE_bf16( float(y[m][k mod N]) * scale )  for 0 <= k < n_next
+ * from the BF16 value just stored, so x_next is bitwise what
+ * sgemm_bf16_rescale would make from y (vLLM PR #65306, Validation, and its
+ * decode-chain protocol: one GEMM per projection, the next input formed from
+ * the previous output).  Saves one kernel launch per GEMM of the chain.
+ * - x_next: DEVICE array, row stride ld_next >= n_next elements, 2-byte aligned,
+ *   overlapping none of x, W and y (else SGEMM_ERR_INVALID_ARG; the kernel
+ *   still reads x and W while it writes x_next).  1 <= n_next < 2^31.
+ * - With SGEMM_FLAG_PDL the next GEMM on the stream waits for this one before it
+ *   reads x_next, as for y.  Other arguments and errors as sgemm_bf16_skinny_ex. */
+sgemm_status_t sgemm_bf16_skinny_rescale_ex(const sgemm_bf16_t *x, long long ldx,
+                                            const sgemm_bf16_t *W, sgemm_bf16_t *y, long long ldy,
+                                            int M, int N, int K, sgemm_bf16_t *x_next,
+                                            long long ld_next, long long n_next, float scale,
+                                            const sgemm_plan_t *plan, unsigned flags,
+                                            sgemm_stream_t stream);
+
+/* y = x . W^T with FP32 outputs: the FP32 sums are stored without rounding to
+ * BF16.  For projections whose consumer wants FP32, such as the MoE router gate
+ * (288, 4096) that vLLM PR #62949 (Validation, the nsys census) leaves on cuBLAS
+ * because of its FP32 output.  Same kernels, plans and accumulation order as
+ * sgemm_bf16_skinny_ex; y is a DEVICE array of float, row stride ldy >= N
+ * elements, 4-byte aligned (else SGEMM_ERR_MISALIGNED).  Other arguments and
+ * errors as sgemm_bf16_skinny_ex. */
+sgemm_status_t sgemm_bf16_skinny_f32out_ex(const sgemm_bf16_t *x, long long ldx,
+                                           const sgemm_bf16_t *W, float *y, long long ldy, int M,
+                                           int N, int K, const sgemm_plan_t *plan, unsigned flags,
+                                           sgemm_stream_t stream);
+
 sgemm_status_t sgemm_bf16_rescale(const sgemm_bf16_t *y, long long n_src, sgemm_bf16_t *x,
                                   long long n_dst, float scale, unsigned flags,
                                   sgemm_stream_t stream);

@@ -9,7 +9,7 @@ The arithmetic lives in ``skinny_oracle.c`` (plain C, exact fixed-point
 accumulation, one round-to-nearest-even to BF16 at the end; the header of that
 file states the definition and cites the pages it follows).  This module only
 builds it with gcc, loads it with ctypes and marshals numpy arrays of raw BF16
-bits (``uint16``).
+bits (``uint16``); the FP32-output form returns FP32 bit patterns (``uint32``).
 
 Parity status: pinned.  ``tests/test_oracle_pins.py`` checks it against an
 independent brute-force rounding of exact rational sums, hand-derived closed
@@ -70,6 +70,9 @@ class Oracle:
         ci = ctypes.c_int
         lib.oracle_bf16_skinny_gemm.argtypes = [u16p, ll, u16p, ll, u16p, ll, ci, ci, ci, ci]
         lib.oracle_bf16_skinny_gemm.restype = ci
+        u32p = ctypes.POINTER(ctypes.c_uint32)
+        lib.oracle_bf16_skinny_gemm_f32.argtypes = [u16p, ll, u16p, ll, u32p, ll, ci, ci, ci, ci]
+        lib.oracle_bf16_skinny_gemm_f32.restype = ci
         lib.oracle_exact_dot.argtypes = [u16p, u16p, ci, i64p, ip, ip]
         lib.oracle_exact_dot.restype = ctypes.c_uint16
         lib.oracle_cores.restype = ci
@@ -108,6 +111,23 @@ class Oracle:
         if used < 0:
             raise ValueError("oracle rejected its arguments")
         return (y, used) if return_threads else y
+
+    def skinny_gemm_f32(self, x_bits, W_bits, threads: int = 0):
+        """FP32 bit patterns (uint32) [M,N]: RNE_fp32 of each exact dot product."""
+        x = np.ascontiguousarray(_u16(x_bits))
+        W = np.ascontiguousarray(_u16(W_bits))
+        if x.ndim != 2 or W.ndim != 2 or x.shape[1] != W.shape[1]:
+            raise ValueError(f"shapes x{x.shape} W{W.shape} do not form x @ W^T")
+        M, K = x.shape
+        N = W.shape[0]
+        y = np.zeros((M, N), dtype=np.uint32)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        used = self._lib.oracle_bf16_skinny_gemm_f32(
+            x.ctypes.data_as(u16p), K, W.ctypes.data_as(u16p), K,
+            y.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)), N, M, N, K, int(threads))
+        if used < 0:
+            raise ValueError("oracle rejected its arguments")
+        return y
 
     def exact_dot(self, x_row, w_row):
         """Exact dot product of two BF16 rows.
@@ -152,6 +172,11 @@ def default() -> Oracle:
 def skinny_gemm(x_bits, W_bits, threads: int = 0, return_threads: bool = False):
     """See :meth:`Oracle.skinny_gemm`."""
     return default().skinny_gemm(x_bits, W_bits, threads, return_threads)
+
+
+def skinny_gemm_f32(x_bits, W_bits, threads: int = 0):
+    """See :meth:`Oracle.skinny_gemm_f32`."""
+    return default().skinny_gemm_f32(x_bits, W_bits, threads)
 
 
 def exact_dot(x_row, w_row):

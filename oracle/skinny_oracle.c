@@ -19,8 +19,13 @@
  *    output element with a float64 reference.  Here the sum is not merely
  *    float64 but exact, so the oracle has no rounding-order freedom at all:
  *    the only rounding is the final one to BF16.
- *  - Rounding to BF16 is round-to-nearest, ties-to-even (the pages only say
- *    "BF16 output"; RNE is the IEEE default and the CUDA/PyTorch convention).
+ *  - Rounding to BF16 is round-to-nearest, ties-to-even (the pages give BF16
+ *    outputs without a rounding mode; RNE is the IEEE default and the
+ *    CUDA/PyTorch convention).
+ *  - The FP32-output form (oracle_bf16_skinny_gemm_f32) rounds the same exact
+ *    sum once to FP32, round-to-nearest, ties-to-even: the outputs of the MoE
+ *    router gate (288, 4096), which vLLM PR #62949 (Validation, the nsys
+ *    census) names as the one projection kept in FP32.
  *
  * Exactness.  A finite BF16 value is s * 2^e with an integer significand
  * 0 <= s <= 255 and -133 <= e <= 120.  A product of two of them is
@@ -225,6 +230,23 @@ static uint16_t acc_to_bf16(exact_acc *a) {
     return (uint16_t)(s | ((uint32_t)(u + 134) << 7) | (uint32_t)(q - 128));
 }
 
+/* final FP32 bits of the accumulated sum: 24 significand bits, smallest ulp
+ * 2^-149, largest finite value (2^24 - 1) * 2^104 */
+static uint32_t acc_to_f32(exact_acc *a) {
+    if (a->nan || (a->pinf && a->ninf)) return 0x7fc00000u;
+    if (a->pinf) return 0x7f800000u;
+    if (a->ninf) return 0xff800000u;
+    int sign = acc_normalize(a);
+    if (sign == 0) return 0x00000000u;
+    uint64_t q;
+    int u;
+    acc_round(a, 24, -149, &q, &u);
+    uint32_t s = sign < 0 ? 0x80000000u : 0u;
+    if (q < ((uint64_t)1 << 23)) return s | (uint32_t)q;          /* subnormal (u == -149) */
+    if (u > 104) return s | 0x7f800000u;                           /* q*2^u >= 2^128: overflow */
+    return s | ((uint32_t)(u + 150) << 23) | (uint32_t)(q - ((uint64_t)1 << 23));
+}
+
 /* ---- exported entry points -------------------------------------------------- */
 
 /* Number of CPUs this process may run on. */
@@ -240,7 +262,8 @@ int oracle_cores(void) {
 
 typedef struct {
     const uint16_t *x, *W;
-    uint16_t *y;
+    uint16_t *y;       /* BF16 outputs, or */
+    uint32_t *y32;     /* FP32 outputs (bit patterns) when non-null */
     long long ldx, ldw, ldy;
     int M, K, n0, n1;
     const bf16_parts *xp; /* decoded x, M*K */
@@ -259,22 +282,20 @@ static void *run_rows(void *arg) {
                 bf16_parts wp = decode_bf16(wrow[k]);
                 acc_mac(&acc, &xr[k], &wp);
             }
-            j->y[(long long)m * j->ldy + n] = acc_to_bf16(&acc);
+            if (j->y32)
+                j->y32[(long long)m * j->ldy + n] = acc_to_f32(&acc);
+            else
+                j->y[(long long)m * j->ldy + n] = acc_to_bf16(&acc);
         }
     }
     return NULL;
 }
 
-/* y[m*ldy + n] = RNE_bf16(exact sum_k x[m*ldx + k] * W[n*ldw + k])
- * for 0 <= m < M, 0 <= n < N.  All arrays hold raw BF16 bits in host memory.
- * threads <= 0 uses every CPU in the affinity mask.  Rows n are split into
- * contiguous ranges, one per thread; the result does not depend on the
- * thread count.  Returns the number of threads used, or -1 on bad arguments. */
-int oracle_bf16_skinny_gemm(const uint16_t *x, long long ldx, const uint16_t *W, long long ldw,
-                            uint16_t *y, long long ldy, int M, int N, int K, int threads) {
+static int gemm(const uint16_t *x, long long ldx, const uint16_t *W, long long ldw, uint16_t *y,
+                uint32_t *y32, long long ldy, int M, int N, int K, int threads) {
     if (M < 0 || N < 0 || K < 0 || K >= ACC_MAX_K) return -1;
     if (M == 0 || N == 0) return 0;
-    if (!x || !W || !y || ldx < K || ldw < K || ldy < N) return -1;
+    if (!x || !W || (!y && !y32) || ldx < K || ldw < K || ldy < N) return -1;
     if (threads <= 0) threads = oracle_cores();
     if (threads > N) threads = N;
     bf16_parts *xp = (bf16_parts *)malloc(sizeof(bf16_parts) * (size_t)M * (size_t)(K ? K : 1));
@@ -293,6 +314,7 @@ int oracle_bf16_skinny_gemm(const uint16_t *x, long long ldx, const uint16_t *W,
         jobs[t].x = x;
         jobs[t].W = W;
         jobs[t].y = y;
+        jobs[t].y32 = y32;
         jobs[t].ldx = ldx;
         jobs[t].ldw = ldw;
         jobs[t].ldy = ldy;
@@ -317,6 +339,25 @@ int oracle_bf16_skinny_gemm(const uint16_t *x, long long ldx, const uint16_t *W,
     free(jobs);
     free(tids);
     return threads;
+}
+
+/* y[m*ldy + n] = RNE_bf16(exact sum_k x[m*ldx + k] * W[n*ldw + k])
+ * for 0 <= m < M, 0 <= n < N.  All arrays hold raw BF16 bits in host memory.
+ * threads <= 0 uses every CPU in the affinity mask.  Rows n are split into
+ * contiguous ranges, one per thread; the result does not depend on the
+ * thread count.  Returns the number of threads used, or -1 on bad arguments. */
+int oracle_bf16_skinny_gemm(const uint16_t *x, long long ldx, const uint16_t *W, long long ldw,
+                            uint16_t *y, long long ldy, int M, int N, int K, int threads) {
+    if (!y) return -1;
+    return gemm(x, ldx, W, ldw, y, NULL, ldy, M, N, K, threads);
+}
+
+/* The same sums rounded once to FP32 (RNE): y holds FP32 bit patterns. */
+int oracle_bf16_skinny_gemm_f32(const uint16_t *x, long long ldx, const uint16_t *W,
+                                long long ldw, uint32_t *y, long long ldy, int M, int N, int K,
+                                int threads) {
+    if (!y) return -1;
+    return gemm(x, ldx, W, ldw, NULL, y, ldy, M, N, K, threads);
 }
 
 /* The exact dot product of one x row and one W row, for tests that need the

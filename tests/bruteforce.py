@@ -54,6 +54,40 @@ def round_bf16(v: Fraction) -> int:
     return sign | (lo if lo % 2 == 0 else hi)
 
 
+_F32_MAX = (Fraction(2) ** 24 - 1) * Fraction(2) ** 104
+
+
+def round_f32(v: Fraction) -> int:
+    """FP32 bits of the exact rational ``v`` under roundTiesToEven, by exact
+    integer arithmetic: find the binade, scale so the ulp is 1, round the
+    quotient half to even, carry into the next binade, and overflow to +-inf
+    at or beyond the midpoint between the largest finite value and 2^128."""
+    if v == 0:
+        return 0x00000000
+    sign = 0x80000000 if v < 0 else 0
+    a = abs(v)
+    if a >= (_F32_MAX + Fraction(2) ** 128) / 2:
+        return sign | 0x7F800000
+    e = a.numerator.bit_length() - a.denominator.bit_length()   # 2^e <= a < 2^(e+2)
+    if Fraction(2) ** e > a:
+        e -= 1
+    if Fraction(2) ** (e + 1) <= a:
+        e += 1
+    u = max(e - 23, -149)                      # exponent of the ulp
+    q = a / Fraction(2) ** u
+    qi = q.numerator // q.denominator
+    rem = q - qi
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and qi % 2 == 1):
+        qi += 1
+    if qi == 1 << 24:                           # carried into the next binade
+        qi, u = 1 << 23, u + 1
+    if u > 104:
+        return sign | 0x7F800000
+    if qi < (1 << 23):                          # subnormal
+        return sign | qi
+    return sign | ((u + 150) << 23) | (qi - (1 << 23))
+
+
 def exact_dot(x_row, w_row):
     """Exact sum of products: a Fraction, or 'nan' / '+inf' / '-inf'."""
     xs = [bf16_to_float(b) for b in x_row]
@@ -66,6 +100,25 @@ def exact_dot(x_row, w_row):
             return "nan"
         return "+inf" if s > 0 else "-inf"
     return sum((Fraction(a) * Fraction(b) for a, b in zip(xs, ws)), Fraction(0))
+
+
+def gemm_f32(x_bits: np.ndarray, W_bits: np.ndarray):
+    """(y FP32 bits [M,N] as uint32, nan mask [M,N]) for tiny inputs."""
+    M, N = x_bits.shape[0], W_bits.shape[0]
+    y = np.zeros((M, N), dtype=np.uint32)
+    nan = np.zeros((M, N), dtype=bool)
+    for m in range(M):
+        for n in range(N):
+            s = exact_dot(x_bits[m], W_bits[n])
+            if s == "nan":
+                nan[m, n] = True
+            elif s == "+inf":
+                y[m, n] = 0x7F800000
+            elif s == "-inf":
+                y[m, n] = 0xFF800000
+            else:
+                y[m, n] = round_f32(s)
+    return y, nan
 
 
 def gemm(x_bits: np.ndarray, W_bits: np.ndarray):

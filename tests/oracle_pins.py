@@ -12,6 +12,11 @@ Each ``pin_*`` takes a loaded :class:`oracle.Oracle` and raises
   of the exact sum, independence of the thread count),
 - a float64 library matmul (agreement up to one BF16 ulp, nearly always exact).
 
+The FP32-output form of the oracle has pins of its own (``pin_f32_*``): the
+brute force's exact-integer FP32 rounding on tiny inputs, hand-derived ties,
+overflow and subnormal cases, negation and power-of-two scaling, and a float64
+library matmul converted to float32.
+
 The same pins run against copies of the oracle with planted mistakes, which
 must fail at least one of them (``test_oracle_pins.py``).
 """
@@ -215,7 +220,100 @@ def pin_float64_library(orc):
     assert np.all(d <= ulp_bf16(bits_to_f64(y))), "float64 library differs by more than one ulp"
 
 
+# ------------------------------------------------------------ FP32 outputs
+def _f32_nan(y):
+    return ((y & 0x7F800000) == 0x7F800000) & ((y & 0x007FFFFF) != 0)
+
+
+def _f32_values(y):
+    return np.asarray(y, np.uint32).view(np.float32).astype(np.float64)
+
+
+def pin_f32_bruteforce_wild(orc, seeds=range(12)):
+    """FP32 outputs against the brute force's exact-integer rounding, with
+    cancellation, huge values (overflow to inf) and subnormal inputs."""
+    for s in seeds:
+        rng = _rng(5000 + s)
+        M, N = 1 + s % 4, 1 + (5 * s) % 7
+        K = [1, 2, 3, 8, 16, 31, 48, 64, 5, 40, 24, 7][s % 12]
+        lo, hi = ((120, 134) if s % 2 else (60, 200))
+        x = wild_bits(rng, (M, K), lo, hi)
+        W = wild_bits(rng, (N, K), lo, hi)
+        y = orc.skinny_gemm_f32(x, W)
+        yb, nb = bruteforce.gemm_f32(x, W)
+        _same(y, _f32_nan(y), yb, nb, f"FP32 brute force (seed {s}, M{M} N{N} K{K})")
+
+
+def pin_f32_bruteforce_subnormal_region(orc, seeds=range(4)):
+    """Products landing around the FP32 subnormal range (units of 2^-149)."""
+    for s in seeds:
+        rng = _rng(6000 + s)
+        x = wild_bits(rng, (2, 10), 48, 66, p_sub=0.1, p_huge=0.0)
+        W = wild_bits(rng, (4, 10), 48, 66, p_sub=0.1, p_huge=0.0)
+        y = orc.skinny_gemm_f32(x, W)
+        yb, nb = bruteforce.gemm_f32(x, W)
+        _same(y, _f32_nan(y), yb, nb, f"FP32 subnormal region (seed {s})")
+
+
+def pin_f32_closed_forms(orc):
+    """Hand-derived FP32 results (BF16 bits: 1 = 0x3F80, 2^-24 = 0x3380, 2^-30 =
+    0x3080, 1 + 2^-7 = 0x3F81, 2^127 = 0x7F00, 4 = 0x4080, 2 - 2^-7 = 0x3FFF,
+    2^-75 = 0x1A00, 1.5 * 2^-75 = 0x1A40)."""
+    cases = [
+        # 1 + 2^-24: exactly half an FP32 ulp above 1, ties to the even 1.0
+        ([0x3F80, 0x3F80], [0x3F80, 0x3380], 0x3F800000),
+        # 1 + 2^-24 + 2^-30: above the midpoint, rounds up to 1 + 2^-23
+        ([0x3F80] * 3, [0x3F80, 0x3380, 0x3080], 0x3F800001),
+        # (1 + 2^-7) + 2^-24: a tie again; 0x3F810000 has an even significand, so it stays
+        ([0x3F80, 0x3F80], [0x3F81, 0x3380], 0x3F810000),
+        # 2^127 * 4 = 2^129 overflows to +inf
+        ([0x7F00], [0x4080], 0x7F800000),
+        # 2^127 * (2 - 2^-7) = 2^128 - 2^120: 8 significand bits, exact, finite
+        ([0x7F00], [0x3FFF], 0x7F7F0000),
+        # 2^-150: half the smallest subnormal 2^-149, ties to the even +0
+        ([0x1A00], [0x1A00], 0x00000000),
+        # 1.5 * 2^-150 = 0.75 * 2^-149: rounds to the smallest subnormal
+        ([0x1A00], [0x1A40], 0x00000001),
+        # -(1 + 2^-24 + 2^-30): the sign does not change the magnitude's rounding
+        ([0xBF80] * 3, [0x3F80, 0x3380, 0x3080], 0xBF800001),
+    ]
+    for xs, ws, expect in cases:
+        y = orc.skinny_gemm_f32(np.array([xs], np.uint16), np.array([ws], np.uint16))
+        assert y[0, 0] == expect, f"FP32 closed form {xs}.{ws}: {y[0, 0]:#010x} != {expect:#010x}"
+    # 12289 ones: exact in FP32 (BF16 would give 12288); encoded by the host's float32
+    one = np.full((1, 12289), 0x3F80, np.uint16)
+    expect = int(np.array([12289.0], np.float32).view(np.uint32)[0])
+    assert orc.skinny_gemm_f32(one, one)[0, 0] == expect, "sum of 12289 ones"
+
+
+def pin_f32_negation_and_scaling(orc):
+    x_t = synth.normal_bf16((2, 640), 1.0, seed=41)
+    W = synth.bits(synth.normal_bf16((20, 640), 0.02, seed=42))
+    y1 = _f32_values(orc.skinny_gemm_f32(synth.bits(x_t), W))
+    y_neg = _f32_values(orc.skinny_gemm_f32(synth.bits(x_t) ^ np.uint16(0x8000), W))
+    assert np.array_equal(y_neg, -y1), "negating x did not negate the FP32 outputs"
+    for j in (-9, 5):
+        xs = (x_t.double() * 2.0 ** j).to(torch.bfloat16)
+        y2 = _f32_values(orc.skinny_gemm_f32(synth.bits(xs), W))
+        assert np.array_equal(y2, y1 * 2.0 ** j), f"scaling x by 2^{j} did not scale y"
+
+
+def pin_f32_float64_library(orc):
+    """A float64 library matmul converted to float32 agrees within one FP32 ulp
+    and nearly always bitwise (float64 keeps 29 more bits than FP32)."""
+    xt = synth.normal_bf16((4, 4096), 1.0, seed=43)
+    Wt = synth.normal_bf16((288, 4096), 0.02, seed=44)
+    y = orc.skinny_gemm_f32(synth.bits(xt), synth.bits(Wt))
+    lib = (xt.double() @ Wt.double().T).numpy().astype(np.float32).view(np.uint32)
+    frac_equal = float(np.mean(lib == y))
+    assert frac_equal >= 0.999, f"only {frac_equal:.4f} of FP32 outputs equal the library's"
+    d = np.abs(lib.astype(np.int64) - y.astype(np.int64))   # same sign here: ulps apart
+    assert np.all(d <= 1), "float64 library differs by more than one FP32 ulp"
+
+
 ALL_PINS = [pin_golden, pin_bruteforce_wild, pin_bruteforce_subnormal_region,
             pin_bruteforce_gaussian, pin_exact_sum, pin_large_constant, pin_k_permutation,
             pin_row_permutation, pin_scaling, pin_negation, pin_rows_independent,
-            pin_linearity, pin_threads, pin_float64_library]
+            pin_linearity, pin_threads, pin_float64_library,
+            pin_f32_bruteforce_wild, pin_f32_bruteforce_subnormal_region, pin_f32_closed_forms,
+            pin_f32_negation_and_scaling, pin_f32_float64_library]

@@ -86,6 +86,36 @@ def test_bad_strides_and_alignment_rejected(lib):
     assert _call(lib, A16, A16, A16 + 1, 1, 16, 64) == sk.SGEMM_ERR_MISALIGNED
 
 
+def test_fused_chain_epilogue_argument_checks(lib):
+    X, W, Y, XN = 0x10000, 0x20000, 0x30000, 0x40000
+
+    def call(xn, ldn, n_next, y=Y, x=X):
+        return lib.sgemm_bf16_skinny_rescale_ex(x, 64, W, y, 16, 2, 16, 64, xn, ldn, n_next, 0.5,
+                                                None, 0, None)
+    assert call(NULL, 64, 64) == sk.SGEMM_ERR_INVALID_ARG
+    assert call(XN, 64, 0) == sk.SGEMM_ERR_INVALID_ARG            # n_next < 1
+    assert call(XN, 32, 64) == sk.SGEMM_ERR_INVALID_ARG           # row stride < n_next
+    assert call(XN, 64, 1 << 31) == sk.SGEMM_ERR_INVALID_ARG      # n_next must fit an int
+    assert call(XN + 1, 64, 64) == sk.SGEMM_ERR_MISALIGNED
+    # x_next may overlap none of x, W and y: the kernel still reads x and W
+    assert call(X + 64, 64, 64) == sk.SGEMM_ERR_INVALID_ARG       # inside x
+    assert call(W + 2 * 16 * 64 - 2, 64, 64) == sk.SGEMM_ERR_INVALID_ARG  # last W element
+    assert call(Y, 64, 64) == sk.SGEMM_ERR_INVALID_ARG
+    assert call(X - 2 * (64 + 64) + 2, 64, 64) == sk.SGEMM_ERR_INVALID_ARG  # ends inside x
+    # the problem's own checks still come first
+    assert lib.sgemm_bf16_skinny_rescale_ex(X, 64, W, Y, 16, 5, 16, 64, XN, 64, 64, 0.5, None, 0,
+                                            None) == sk.SGEMM_ERR_INVALID_ARG
+
+
+def test_fp32_output_argument_checks(lib):
+    X, W, Y = 0x10000, 0x20000, 0x30000
+    f = lib.sgemm_bf16_skinny_f32out_ex
+    assert f(X, 64, W, Y + 2, 16, 1, 16, 64, None, 0, None) == sk.SGEMM_ERR_MISALIGNED
+    assert f(X, 64, W, NULL, 16, 1, 16, 64, None, 0, None) == sk.SGEMM_ERR_INVALID_ARG
+    assert f(X, 64, W, Y, 15, 2, 16, 64, None, 0, None) == sk.SGEMM_ERR_INVALID_ARG
+    assert f(X, 64, W, Y, 16, 1, 16, 60, None, 0, None) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE
+
+
 def test_unknown_flags_rejected(lib):
     assert lib.sgemm_bf16_skinny_ex(A16, 64, A16, A16, 16, 1, 16, 64, None, 8, None) == \
         sk.SGEMM_ERR_INVALID_ARG

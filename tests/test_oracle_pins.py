@@ -55,6 +55,17 @@ MUTANTS = [
      [("if (u > 120) return (uint16_t)(s | 0x7f80);", "")]),
     ("inf_times_zero_not_nan",
      [("if (other == 0)\n            a->nan = 1;", "if (0)\n            a->nan = 1;")]),
+    ("f32_one_bit_short",
+     [("acc_round(a, 24, -149, &q, &u);", "acc_round(a, 23, -149, &q, &u);")]),
+    ("f32_exponent_bias_off_by_one",
+     [("return s | ((uint32_t)(u + 150) << 23)", "return s | ((uint32_t)(u + 151) << 23)")]),
+    ("f32_no_overflow_to_inf",
+     [("if (u > 104) return s | 0x7f800000u;", "")]),
+    ("f32_flush_subnormals",
+     [("if (q < ((uint64_t)1 << 23)) return s | (uint32_t)q;", "if (q < ((uint64_t)1 << 23)) return s;")]),
+    ("f32_rounded_through_bf16",
+     [("j->y32[(long long)m * j->ldy + n] = acc_to_f32(&acc);",
+       "j->y32[(long long)m * j->ldy + n] = (uint32_t)acc_to_bf16(&acc) << 16;")]),
 ]
 
 

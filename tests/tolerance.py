@@ -26,6 +26,12 @@ Two per-element bounds and one per-row cosine, all evaluated in float64:
 
 Non-finite references must be matched in kind (NaN by NaN, +-inf by the same
 infinity).
+
+FP32 outputs (``compare_f32``): the GPU's FP32 sum differs from the exact sum by
+at most e (bound 2), and the oracle's reference is the exact sum rounded once
+to FP32, so |y_gpu - y_ref| <= e + ulp_f32(|y_ref|) / 2; the cosine check is the
+same.  The spec element bound is stated for BF16 outputs and does not
+apply.
 """
 from __future__ import annotations
 
@@ -129,4 +135,51 @@ def compare(y_gpu_bits, y_ref_bits, x_bits, W_bits, *, tight: bool = True,
 
     rep["ok"] = bool(rep["bad_kind"] == 0 and not ns_bad.any() and not t_bad.any()
                      and (cos_min >= 0.99999 or not cosine))
+    return rep
+
+
+def f32_bits_to_f64(b: np.ndarray) -> np.ndarray:
+    """Raw FP32 bits (uint32) -> exact float64 values."""
+    return np.asarray(b, dtype=np.uint32).view(np.float32).astype(np.float64)
+
+
+def ulp_f32(v: np.ndarray) -> np.ndarray:
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    out = np.full(a.shape, 2.0 ** -149)
+    normal = a >= 2.0 ** -126
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(normal, a, 1.0)))
+    out[normal] = np.exp2(e[normal] - 23)
+    return out
+
+
+def compare_f32(y_gpu_bits, y_ref_bits, x_bits, W_bits) -> dict:
+    """Check an FP32-output GEMM against the oracle's FP32 reference (bits as uint32)."""
+    g = f32_bits_to_f64(y_gpu_bits)
+    r = f32_bits_to_f64(y_ref_bits)
+    K = np.asarray(x_bits).shape[1]
+    rep = {"ok": True, "n": int(r.size), "K": int(K)}
+    ref_fin = np.isfinite(r)
+    bad_kind = (~ref_fin) & ~((np.isnan(r) & np.isnan(g)) | (r == g))
+    bad_kind |= ref_fin & ~np.isfinite(g)
+    rep["bad_kind"] = int(bad_kind.sum())
+    with np.errstate(invalid="ignore"):
+        diff = np.where(ref_fin & np.isfinite(g), np.abs(g - r), 0.0)
+    e = gamma(max(K - 1, 0)) * abs_dot(x_bits, W_bits) + K * 2.0 ** -150
+    tol = e + 0.5 * ulp_f32(r)
+    bad = ref_fin & (diff > tol)
+    rep["violations"] = int(bad.sum())
+    rep["max_err_over_tol"] = float(np.max(np.where(ref_fin, diff / tol, 0.0), initial=0.0))
+    rep["bitwise_equal_frac"] = float(np.mean(np.asarray(y_gpu_bits) == np.asarray(y_ref_bits))) \
+        if r.size else 1.0
+    cos_min = 1.0
+    for m in range(r.shape[0]):
+        sel = ref_fin[m] & np.isfinite(g[m])
+        a, b = g[m][sel], r[m][sel]
+        na, nb = np.linalg.norm(a), np.linalg.norm(b)
+        c = 1.0 if (na == 0.0 and nb == 0.0) else (0.0 if na == 0.0 or nb == 0.0
+                                                    else float(np.dot(a, b) / (na * nb)))
+        cos_min = min(cos_min, c)
+    rep["cosine_min"] = cos_min
+    rep["ok"] = bool(rep["bad_kind"] == 0 and not bad.any() and cos_min >= 0.99999)
     return rep
