@@ -21,7 +21,7 @@ Reported (one JSON line on rank 0):
 ``--impl reference`` times the CPU oracle alone (the reference arm).
 ``--workload`` selects other configurations: single, lmhead, pairs, chain (with
 the elementwise step separate and fused into the GEMM epilogue), router (the
-FP32-output router gate).
+FP32-output router gate), wide (M = 5..8, with cuBLAS timed beside for context).
 """
 from __future__ import annotations
 
@@ -672,13 +672,90 @@ def run_router(args, torch, sk, synth, dist, min_bytes):
     return 0
 
 
+def run_wide(args, torch, sk, synth, dist, min_bytes):
+    """Wider batches, M = 5..8 (speculative verification), over the sweep shapes:
+    each (N, K, M) a CUDA graph of R GEMMs on R weight copies (cold), through
+    sgemm_bf16_skinny_ex with the selected plan.  For context only, the same
+    graphs through torch's F.linear (cuBLAS), which is where vLLM PR #62949
+    (Validation) leaves M = 8; nothing of this library runs in that column."""
+    import torch.nn.functional as F
+    ws, rank, _ = dist_info()
+    dev = torch.device("cuda")
+    flags = sk.SGEMM_FLAG_PDL | sk.SGEMM_FLAG_WEIGHTS_READONLY
+    ms = [int(v) for v in args.ms.split(",")] if args.ms else [5, 6, 7, 8]
+    shapes = SWEEP_SHAPES
+    if args.shapes:
+        shapes = [tuple(int(v) for v in t.split("x")) for t in args.shapes.split(",")]
+    detail, graphs, keep, nbytes, launches = [], [], [], 0, 0
+    for (N, K) in shapes:
+        R = max(2, math.ceil(min_bytes / (2 * N * K)))
+        W = torch.empty((R, N, K), dtype=torch.bfloat16, device=dev)
+        for i in range(R):
+            W[i].copy_(synth.normal_bf16((N, K), synth.W_STD, seed=i, device=dev))
+        for M in ms:
+            x = synth.normal_bf16((R, M, K), synth.X_STD, seed=300 + M, device=dev)
+            y = torch.empty((R, M, N), dtype=torch.bfloat16, device=dev)
+            yc = torch.empty((R, M, N), dtype=torch.bfloat16, device=dev)
+            keep.append((W, x, y, yc))
+
+            def ours(W=W, x=x, y=y, R=R):
+                for i in range(R):
+                    sk.sgemm_bf16_skinny_ex(x[i], W[i], y[i], flags=flags)
+
+            def cublas(W=W, x=x, yc=yc, R=R):
+                for i in range(R):
+                    torch.matmul(x[i], W[i].T, out=yc[i])
+
+            ours()
+            cublas()
+            torch.cuda.synchronize()
+            graphs += [_capture(torch, ours), _capture(torch, cublas)]
+            p = sk.sgemm_plan_select(N, K, M)
+            detail.append({"N": N, "K": K, "M": M, "copies": R,
+                           "plan": {"variant": p.variant, "threads": p.threads,
+                                    "k_unroll": p.k_unroll, "split_k": p.split_k, "id": p.id}})
+            nbytes += R * gemm_bytes(M, N, K)
+            launches += R * (2 if p.split_k > 1 and p.variant != sk.SGEMM_VARIANT_MMA_TW else 1)
+    per, _ = _time_graphs(torch, dist, graphs, args.steps, args.warmup)
+    del graphs, keep
+    peak, _ = measured_peaks()
+    total_ms = 0.0
+    for d, (o_ms, c_ms) in zip(detail, zip(per[0::2], per[1::2])):
+        b = gemm_bytes(d["M"], d["N"], d["K"])
+        d["us"] = round(o_ms * 1e3 / d["copies"], 3)
+        d["gbs"] = round(b / (o_ms * 1e3 / d["copies"]) / 1e3, 1)
+        d["frac"] = round(d["gbs"] / peak, 4)
+        d["us_cublas_informational"] = round(c_ms * 1e3 / d["copies"], 3)
+        total_ms += o_ms
+    value = dist.sum(nbytes) / (dist.max(total_ms) / 1e3) / 1e9
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "wide batches M=" + ",".join(map(str, ms)) + " over (N,K) = " +
+                                   ", ".join(f"({n},{k})" for n, k in shapes),
+                       "x": "BF16 ~ N(0,1)", "W": "BF16 ~ N(0,0.02^2)",
+                       "l2": "inputs larger than L2 (rotating weight copies)",
+                       "launch_flags": "pdl,readonly", "parallelism": "replicas"},
+            "gpu_launches": launches * args.steps,
+            "detail": detail}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+        if args.detail_out:
+            with open(args.detail_out, "w") as f:
+                json.dump(line, f, indent=1)
+    dist.close()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["sweep", "single", "lmhead", "pairs", "chain", "router"],
+    ap.add_argument("--workload",
+                    choices=["sweep", "single", "lmhead", "pairs", "chain", "router", "wide"],
                     default="sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -731,6 +808,8 @@ def main():
         return run_pairs(args, torch, sk, synth, dist, min_bytes)
     elif args.workload == "router":
         return run_router(args, torch, sk, synth, dist, min_bytes)
+    elif args.workload == "wide":
+        return run_wide(args, torch, sk, synth, dist, min_bytes)
     else:
         return run_chain(args, torch, sk, synth, dist)
 

@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) BF16 skinny GEMM: ``y[M,N] = x[M,K] @ W[N,K]^T`` for M = 1..4.
+"""GB300 (sm_103a) BF16 skinny GEMM: ``y[M,N] = x[M,K] @ W[N,K]^T`` for M = 1..8.
 
 A thin ctypes binding over the C ABI of ``libsgemm_skinny.so`` (declared in
 ``include/sgemm_skinny.h``).  The functions keep the C names and only marshal

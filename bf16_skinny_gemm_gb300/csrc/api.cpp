@@ -45,6 +45,10 @@ const KernelInfo *table_for_m(int M) {
         case 2: return sk::kKernelsM2;
         case 3: return sk::kKernelsM3;
         case 4: return sk::kKernelsM4;
+        case 5: return sk::kKernelsM5;
+        case 6: return sk::kKernelsM6;
+        case 7: return sk::kKernelsM7;
+        case 8: return sk::kKernelsM8;
         default: return nullptr;
     }
 }
@@ -141,15 +145,28 @@ sgemm_plan_t make_plan(int variant, int threads, int R, int LPR, int U, int spli
     return p;
 }
 
+// A plan for shapes the table does not hold.  M <= 4: the mixed-precision FMA
+// streaming kernel; M >= 5: the 16-row tensor-core kernel (eight FMAs per
+// element and x row would make the CUDA-core kernel issue-bound).  K is split
+// when the x slice would not leave room for two CTAs per SM, and further while
+// the rows alone give fewer than two CTAs per SM of a GB300 (152 SMs) and each
+// split keeps at least 512 elements of K.
 sgemm_plan_t heuristic_plan(int N, int K, int M) {
-    (void)N;
-    int R, LPR, U;
-    if (K <= 128) {
+    int variant = SGEMM_VARIANT_LDG_MIXFMA;
+    int R, LPR, U, rows_per_cta;
+    if (M >= 5) {
+        variant = SGEMM_VARIANT_MMA;
+        R = 16, LPR = 4, U = 4;
+        rows_per_cta = 16;
+    } else if (K <= 128) {
         R = 2, LPR = 16, U = 2;
+        rows_per_cta = 8 * 2 * R;
     } else if (M <= 2) {
         R = 1, LPR = 32, U = 8;
+        rows_per_cta = 8 * R;
     } else {
         R = 2, LPR = 32, U = 4;
+        rows_per_cta = 8 * R;
     }
     int split = 1;
     const size_t budget = 96 * 1024;  // x slice per CTA, leaves room for two CTAs per SM
@@ -157,8 +174,10 @@ sgemm_plan_t heuristic_plan(int N, int K, int M) {
         const size_t xbytes = static_cast<size_t>(M) * K * 2;
         split = static_cast<int>((xbytes + budget - 1) / budget);
         split = std::max(1, std::min(split, 64));
+        const long long ctas = (static_cast<long long>(std::max(N, 1)) + rows_per_cta - 1) / rows_per_cta;
+        while (split < 16 && ctas * split < 2 * 152 && K / (2 * split) >= 512) split *= 2;
     }
-    return make_plan(SGEMM_VARIANT_LDG_MIXFMA, 256, R, LPR, U, split, 1, 0, -1);
+    return make_plan(variant, 256, R, LPR, U, split, 1, 0, -1);
 }
 
 sgemm_status_t probe_device(int *dev_out, DeviceState **st_out) {
@@ -417,9 +436,9 @@ size_t smem_bytes(const sgemm_plan_t &plan, int M, int kps) {
     if (plan.variant == SGEMM_VARIANT_LDGX_MIXFMA || plan.variant == SGEMM_VARIANT_LDGX_FFMA2)
         return 0;  // x is read from global memory
     if (plan.variant == SGEMM_VARIANT_MMA) {
-        // x rows padded by one chunk, plus two reduction buffers [NW][16][4] floats
+        // x rows padded by one chunk, plus two reduction buffers [NW][16][4 or 8] floats
         return static_cast<size_t>(M) * (chunks + 1) * 16 +
-               2 * static_cast<size_t>(plan.threads / 32) * 16 * 4 * sizeof(float);
+               2 * static_cast<size_t>(plan.threads / 32) * 16 * (M <= 4 ? 4 : 8) * sizeof(float);
     }
     if (plan.variant == SGEMM_VARIANT_MMA_TW) {
         // x rows padded by one chunk, plus two buffers of [NW][32 lanes][2] partial fragments

@@ -1,5 +1,5 @@
 // Internal declarations shared by the host library and the kernel translation
-// units of the BF16 skinny GEMM (y[M,N] = x[M,K] . W[N,K]^T, M <= 4).
+// units of the BF16 skinny GEMM (y[M,N] = x[M,K] . W[N,K]^T, M <= 8).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -11,7 +11,7 @@
 namespace sk {
 
 constexpr int kMaxBatch = SGEMM_MAX_BATCH;
-constexpr int kMaxM = 4;
+constexpr int kMaxM = 8;
 constexpr int kMaxThreads = 256;
 constexpr int kMaxThreadsBulk = 288;  // producer warp + up to 8 consumer warps
 constexpr int kMaxRing = 16;          // ring slots of the bulk-copy kernel
@@ -91,6 +91,10 @@ extern const KernelInfo kKernelsM1[];
 extern const KernelInfo kKernelsM2[];
 extern const KernelInfo kKernelsM3[];
 extern const KernelInfo kKernelsM4[];
+extern const KernelInfo kKernelsM5[];
+extern const KernelInfo kKernelsM6[];
+extern const KernelInfo kKernelsM7[];
+extern const KernelInfo kKernelsM8[];
 extern const int kKernelCountPerM;
 
 // Deterministic split-K reduction kernels, one per M.

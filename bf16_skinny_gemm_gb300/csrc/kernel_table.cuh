@@ -2,7 +2,7 @@
 // (M, rows per lane group R, lanes per row LPR, loads per batch U, FMA mode
 // (0 widened, 1 mixed precision, 2 packed FP32x2, 3 tensor cores on the diagonal of
 // mma.sync), double-buffered batches);
-// every configuration exists for M = 1..4.  The host
+// every configuration exists for M = 1..8.  The host
 // library enumerates these as plans (times two CTA sizes) and the offline
 // sweep times all of them.
 #pragma once

@@ -17,6 +17,10 @@ const void *const kReduceKernels[kMaxM + 1] = {
     reinterpret_cast<const void *>(&splitk_reduce_kernel<2>),
     reinterpret_cast<const void *>(&splitk_reduce_kernel<3>),
     reinterpret_cast<const void *>(&splitk_reduce_kernel<4>),
+    reinterpret_cast<const void *>(&splitk_reduce_kernel<5>),
+    reinterpret_cast<const void *>(&splitk_reduce_kernel<6>),
+    reinterpret_cast<const void *>(&splitk_reduce_kernel<7>),
+    reinterpret_cast<const void *>(&splitk_reduce_kernel<8>),
 };
 
 }  // namespace sk

@@ -1,5 +1,5 @@
 // Tensor-core variant of the weight-streaming skinny GEMM (sm_103a):
-// y[M,N] = x[M,K] . W[N,K]^T with M <= 4 padded to the 8 columns of one
+// y[M,N] = x[M,K] . W[N,K]^T with M <= 8 padded to the 8 columns of one
 // mma.sync m16n8k16 (BF16 inputs, FP32 accumulation).
 //
 // Why: at M = 4 the CUDA-core kernel spends about 100 instructions per KiB of
@@ -38,6 +38,7 @@ namespace sk {
 template <int M, int U, bool DB = false>
 __global__ void __launch_bounds__(kMaxThreads) skinny_mma_kernel(const __grid_constant__ Params p) {
     constexpr int TILE = 16;
+    constexpr int MC = M <= 4 ? 4 : 8;  // columns of a partial tile in shared memory
     extern __shared__ uint4 smem[];
 
     const bool pdl = (p.flags & kFlagPdl) != 0;
@@ -50,7 +51,7 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mma_kernel(const __grid_co
     const int nchunk = kc >> 3;            // 16-byte chunks of this split's K range
     const int xstride = nchunk + 1;        // x row stride in chunks (+1 avoids bank conflicts)
     uint4 *xs = smem;                      // [M][xstride]
-    float *red = reinterpret_cast<float *>(smem + M * xstride);  // [2][NW][TILE][4]
+    float *red = reinterpret_cast<float *>(smem + M * xstride);  // [2][NW][TILE][MC]
 
     const int NW = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5;
@@ -126,13 +127,13 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mma_kernel(const __grid_co
                 if (++ci == I) {
                     // tile done: partial sums of this warp -> shared memory, then the
                     // first 16*M threads add the NW partials in warp order
-                    float *rw = red + (rb * NW + warp) * TILE * 4;
+                    float *rw = red + (rb * NW + warp) * TILE * MC;
                     if (2 * c < M) {
-                        rw[g * 4 + 2 * c] = acc[0];
-                        rw[(g + 8) * 4 + 2 * c] = acc[2];
+                        rw[g * MC + 2 * c] = acc[0];
+                        rw[(g + 8) * MC + 2 * c] = acc[2];
                         if (2 * c + 1 < M) {
-                            rw[g * 4 + 2 * c + 1] = acc[1];
-                            rw[(g + 8) * 4 + 2 * c + 1] = acc[3];
+                            rw[g * MC + 2 * c + 1] = acc[1];
+                            rw[(g + 8) * MC + 2 * c + 1] = acc[3];
                         }
                     }
                     __syncthreads();
@@ -140,9 +141,9 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mma_kernel(const __grid_co
                         const int row = threadIdx.x / M;
                         const int m = threadIdx.x - row * M;
                         const int n = ct * TILE + row;
-                        const float *rr = red + rb * NW * TILE * 4 + row * 4 + m;
+                        const float *rr = red + rb * NW * TILE * MC + row * MC + m;
                         float v = 0.0f;
-                        for (int w = 0; w < NW; ++w) v += rr[w * TILE * 4];
+                        for (int w = 0; w < NW; ++w) v += rr[w * TILE * MC];
                         if (n < p.N) {
                             if (p.split == 1) {
                                 store_out(p, it, m, n, v);

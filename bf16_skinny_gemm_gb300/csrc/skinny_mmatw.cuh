@@ -1,5 +1,5 @@
 // Tensor-core skinny GEMM with warp-owned tiles (sm_103a):
-// y[M,N] = x[M,K] . W[N,K]^T, M <= 4, BF16 in, FP32 accumulation, BF16 out.
+// y[M,N] = x[M,K] . W[N,K]^T, M <= 8, BF16 in, FP32 accumulation, BF16 out.
 //
 // The math is that of skinny_mmat.cuh: x is the A operand of mma.sync
 // m16n8k16 (rows m < M, zero-padded to 16), 8 rows of W the B operand, and

@@ -52,6 +52,10 @@ const sk::KernelInfo *find(int M, const sgemm_plan_t &p) {
         case 2: t = sk::kKernelsM2; break;
         case 3: t = sk::kKernelsM3; break;
         case 4: t = sk::kKernelsM4; break;
+        case 5: t = sk::kKernelsM5; break;
+        case 6: t = sk::kKernelsM6; break;
+        case 7: t = sk::kKernelsM7; break;
+        case 8: t = sk::kKernelsM8; break;
         default: return nullptr;
     }
     const int stages = p.stages == 0 ? 1 : p.stages;
@@ -85,7 +89,8 @@ sgemm_status_t setup_current_device(DeviceSetup **out) {
                 return SGEMM_ERR_CUDA;
             st.scratch = static_cast<float *>(ptr);
             const sk::KernelInfo *tables[] = {sk::kKernelsM1, sk::kKernelsM2, sk::kKernelsM3,
-                                              sk::kKernelsM4};
+                                              sk::kKernelsM4, sk::kKernelsM5, sk::kKernelsM6,
+                                              sk::kKernelsM7, sk::kKernelsM8};
             for (const sk::KernelInfo *t : tables)
                 for (int i = 0; i < sk::kKernelCountPerM; ++i)
                     if (sk::allow_max_dynamic_smem(t[i].fn) != cudaSuccess) return SGEMM_ERR_CUDA;

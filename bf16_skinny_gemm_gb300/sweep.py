@@ -39,7 +39,7 @@ import bf16_skinny_gemm_gb300 as sk
 from bf16_skinny_gemm_gb300 import synth
 
 DECODE_SHAPES = [(12576, 4096), (4096, 4096), (2048, 4096), (4096, 1024), (8192, 1536),
-                 (4096, 8192), (77440, 4096)]
+                 (4096, 8192), (77440, 4096), (288, 4096)]
 PAIR_SHAPE = (4096, 128)
 HERE = os.path.dirname(os.path.abspath(__file__))
 DEFAULT_OUT = os.path.join(HERE, "csrc", "plan_table.inc")

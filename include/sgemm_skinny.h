@@ -1,7 +1,7 @@
 /*
  * sgemm_skinny.h -- C ABI of the GB300 (sm_103a) BF16 skinny GEMM library.
  *
- *     y[M,N] = x[M,K] . W[N,K]^T        1 <= M <= 4, BF16 in, FP32 accumulate, BF16 out
+ *     y[M,N] = x[M,K] . W[N,K]^T        1 <= M <= 8, BF16 in, FP32 accumulate, BF16 out
  *
  * The operation is the F.linear projection of a decode step with M tokens, as
  * used for the unquantized attention, shared-expert and LM-head projections in
@@ -9,6 +9,9 @@
  * projections", Overview and Validation table) and vLLM PR #65306 ("Add SM90
  * skinny GEMM plans for the BF16 decode projections", Overview).  Each weight
  * is read exactly once per call, so the call is bound by HBM bandwidth.
+ * M = 1..4 are the decode widths the pages plan for; M = 5..8 cover wider
+ * batches (speculative verification), which PR #62949 (Validation, below its
+ * cold-L2 table) measured at M = 8 within 2% of cuBLAS and left off its plans.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -60,7 +63,7 @@ typedef struct CUstream_st *sgemm_stream_t;
 
 typedef enum {
     SGEMM_OK = 0,
-    SGEMM_ERR_INVALID_ARG = 1,        /* null pointer, M outside 1..4, N or K < 1, bad ld, batch */
+    SGEMM_ERR_INVALID_ARG = 1,        /* null pointer, M outside 1..8, N or K < 1, bad ld, batch */
     SGEMM_ERR_UNSUPPORTED_SHAPE = 2,  /* K not a multiple of 8, or a plan that cannot run it */
     SGEMM_ERR_MISALIGNED = 3,         /* x or W not 16-byte aligned, ldx % 8 != 0, y odd */
     SGEMM_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */

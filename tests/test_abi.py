@@ -60,7 +60,7 @@ def _call(lib, x, W, y, M, N, K, ldx=None, ldy=None):
 
 @pytest.mark.parametrize("M,N,K,expect", [
     (0, 16, 64, sk.SGEMM_ERR_INVALID_ARG),
-    (5, 16, 64, sk.SGEMM_ERR_INVALID_ARG),
+    (9, 16, 64, sk.SGEMM_ERR_INVALID_ARG),
     (1, 0, 64, sk.SGEMM_ERR_INVALID_ARG),
     (1, 16, 0, sk.SGEMM_ERR_INVALID_ARG),
     (1, 16, 12, sk.SGEMM_ERR_UNSUPPORTED_SHAPE),
@@ -103,7 +103,7 @@ def test_fused_chain_epilogue_argument_checks(lib):
     assert call(Y, 64, 64) == sk.SGEMM_ERR_INVALID_ARG
     assert call(X - 2 * (64 + 64) + 2, 64, 64) == sk.SGEMM_ERR_INVALID_ARG  # ends inside x
     # the problem's own checks still come first
-    assert lib.sgemm_bf16_skinny_rescale_ex(X, 64, W, Y, 16, 5, 16, 64, XN, 64, 64, 0.5, None, 0,
+    assert lib.sgemm_bf16_skinny_rescale_ex(X, 64, W, Y, 16, 9, 16, 64, XN, 64, 64, 0.5, None, 0,
                                             None) == sk.SGEMM_ERR_INVALID_ARG
 
 
@@ -162,7 +162,7 @@ def test_plan_enumeration(lib):
         key = tuple(p.as_dict().items())
         assert key not in seen
         seen.add(key)
-        for M in (1, 2, 3, 4):
+        for M in range(1, 9):
             assert sk.sgemm_plan_check(p, M, 4096, 4096) == sk.SGEMM_OK, p
     with pytest.raises(sk.SgemmError):
         sk.sgemm_plan_get(n)
@@ -173,7 +173,7 @@ SHAPES = [(12576, 4096), (4096, 4096), (2048, 4096), (4096, 1024), (8192, 1536),
 
 
 @pytest.mark.parametrize("N,K", SHAPES)
-@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8])
 def test_selected_plans_are_runnable(lib, N, K, M):
     p = sk.sgemm_plan_select(N, K, M)
     assert sk.sgemm_plan_check(p, M, N, K) == sk.SGEMM_OK, p

@@ -45,7 +45,7 @@ def _f32_bits(t: torch.Tensor) -> np.ndarray:
 
 # ------------------------------------------------------------------ FP32 out
 @pytest.mark.parametrize("N,K", [(288, 4096), (613, 2600)])
-@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8])
 def test_f32_output_every_plan(M, N, K):
     x, W = _inputs(M, N, K, seed=3100 + N + M)
     xd, Wd = x.to(DEV), W.to(DEV)
@@ -112,7 +112,7 @@ def _rescale_cpu(y: torch.Tensor, n_next: int, scale: float) -> torch.Tensor:
 
 @pytest.mark.parametrize("N,K,n_next", [(613, 2600, 1536), (613, 2600, 613), (613, 2600, 2000),
                                         (4096, 1024, 4096), (2048, 4096, 8192)])
-@pytest.mark.parametrize("M", [1, 3])
+@pytest.mark.parametrize("M", [1, 3, 8])
 def test_fused_rescale_every_plan(M, N, K, n_next):
     x, W = _inputs(M, N, K, seed=3300 + N + n_next)
     xd, Wd = x.to(DEV), W.to(DEV)
@@ -213,3 +213,41 @@ def test_fused_decode_chain_equals_separate_steps(flags):
     for i in range(len(seq)):
         assert torch.equal(ys_a[i].view(torch.int16), ys_b[i].view(torch.int16)), i
         assert torch.equal(xs_a[i].view(torch.int16), xs_b[i].view(torch.int16)), i
+
+
+# ------------------------------------------------------ merged projections
+def test_two_projections_of_one_input_in_one_launch():
+    """Two projections of the same x (the f_a/g_a merge of lmdeploy PR #4968,
+    "feat(pytorch): add glm5.3-flash support", Optimizations: merging them cuts
+    the KDA projection launches) in one batched launch, sharing the x buffer,
+    and as one GEMM over the stacked weight [W_a; W_b] with the same plan: both
+    equal the separate calls bitwise."""
+    M, K = 2, 2048
+    Na, Nb = 768, 1280
+    x = synth.normal_bf16((M, K), synth.X_STD, seed=3600).to(DEV)
+    Wa = synth.normal_bf16((Na, K), synth.W_STD, seed=3601).to(DEV)
+    Wb = synth.normal_bf16((Na, K), synth.W_STD, seed=3602).to(DEV)
+    plan = sk.sgemm_plan_select(Na, K, M)
+    ya, yb = sk.sgemm_bf16_skinny_batched_ex([(x, Wa), (x, Wb)], plan=plan)
+    sa = sk.sgemm_bf16_skinny_ex(x, Wa, plan=plan)
+    sb = sk.sgemm_bf16_skinny_ex(x, Wb, plan=plan)
+    torch.cuda.synchronize()
+    assert torch.equal(ya.view(torch.int16), sa.view(torch.int16))
+    assert torch.equal(yb.view(torch.int16), sb.view(torch.int16))
+    # unequal widths: one GEMM over the stacked weight; a CUDA-core plan's order
+    # per output depends only on K and its lanes per row, not on N
+    Wc = synth.normal_bf16((Nb, K), synth.W_STD, seed=3603).to(DEV)
+    stacked = torch.cat([Wa, Wc], 0)
+    plan = sk.sgemm_plan_select(Na + Nb, K, M).copy(variant=sk.SGEMM_VARIANT_LDG_MIXFMA,
+                                                     rows_per_warp=1, lanes_per_row=32,
+                                                     k_unroll=8, split_k=1, stages=1)
+    y = sk.sgemm_bf16_skinny_ex(x, stacked, plan=plan)
+    sa = sk.sgemm_bf16_skinny_ex(x, Wa, plan=plan)
+    sc = sk.sgemm_bf16_skinny_ex(x, Wc, plan=plan)
+    torch.cuda.synchronize()
+    assert torch.equal(y[:, :Na].view(torch.int16), sa.view(torch.int16))
+    assert torch.equal(y[:, Na:].view(torch.int16), sc.view(torch.int16))
+    xb = synth.bits(x.cpu())
+    rep = compare(synth.bits(y), oracle.skinny_gemm(xb, synth.bits(stacked.cpu())), xb,
+                  synth.bits(stacked.cpu()))
+    assert rep["ok"], rep

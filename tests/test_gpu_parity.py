@@ -59,7 +59,7 @@ SMALL = [(1, 8), (1, 64), (7, 264), (33, 128), (300, 1024), (1000, 1536), (517, 
 
 
 @pytest.mark.parametrize("N,K", SMALL)
-@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_small_shapes_default_plan(M, N, K):
     x, W = _inputs(M, N, K, seed=N * 7 + K)
     y = sk.sgemm_bf16_skinny(x.to(DEV), W.to(DEV))
@@ -68,7 +68,7 @@ def test_small_shapes_default_plan(M, N, K):
 
 
 @pytest.mark.parametrize("fam", synth.FAMILIES)
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M", [1, 4, 8])
 def test_input_families(fam, M):
     x, W = _inputs(M, 611, 2048, seed=5, fam=fam)
     y = sk.sgemm_bf16_skinny(x.to(DEV), W.to(DEV))
@@ -82,7 +82,7 @@ def _all_plans():
 
 
 @pytest.mark.parametrize("split", [1, 2, 3, 5])
-@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 6, 8])
 def test_every_plan_every_split(M, split):
     N, K = 613, 2600
     x, W = _inputs(M, N, K, seed=11)
@@ -144,16 +144,17 @@ def test_golden_cases_on_gpu(case):
 
 
 # ----------------------------------------------------------- properties
-def test_deterministic_and_m_independent():
+@pytest.mark.parametrize("MX", [4, 8])
+def test_deterministic_and_m_independent(MX):
     N, K = 4096, 4096
-    x, W = _inputs(4, N, K, seed=13)
+    x, W = _inputs(MX, N, K, seed=13)
     xd, Wd = x.to(DEV), W.to(DEV)
     for p in _all_plans():
         y4 = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=p)
         y4b = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=p)
         torch.cuda.synchronize()
         assert torch.equal(y4.view(torch.int16), y4b.view(torch.int16)), p
-        for m in range(4):
+        for m in range(MX):
             y1 = sk.sgemm_bf16_skinny_ex(xd[m:m + 1], Wd, plan=p)
             torch.cuda.synchronize()
             assert torch.equal(y1.view(torch.int16)[0], y4.view(torch.int16)[m]), (p, m)
@@ -212,7 +213,7 @@ def _sample_rows(N, n=96, seed=0):
 
 
 @pytest.mark.parametrize("N,K", SWEEP_SHAPES + [(77440, 4096)])
-@pytest.mark.parametrize("M", [1, 2, 3, 4])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8])
 def test_full_size_shapes_sampled(M, N, K):
     xd = synth.normal_bf16((M, K), synth.X_STD, seed=100 + M, device=DEV)
     Wd = synth.normal_bf16((N, K), synth.W_STD, seed=200, device=DEV)
