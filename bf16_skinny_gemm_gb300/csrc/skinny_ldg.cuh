@@ -81,60 +81,23 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-// The epilogue of every kernel: output (m, n) of problem `it`, FP32 sum v:
-// y = RNE_bf16(v), or y = v when the outputs are FP32.  Nothing else happens
-// inside the kernels' streaming loops, so the register allocation of those
-// loops does not depend on the rarer epilogue forms.
+// The epilogue of every kernel: output (m, n) of problem `it`, FP32 sum v.
+//  - BF16 output: y = RNE_bf16(v).  With the fused chain epilogue, the next
+//    GEMM's input also gets xn[m][k] = RNE_bf16(float(y) * scale) for every
+//    k < xn_len with k = n (mod N): the elementwise step between the decode
+//    chain's GEMMs, done on the value just rounded, so the result is bitwise
+//    that of the separate step.
+//  - FP32 output: y = v, no rounding.
 __device__ __forceinline__ void store_out(const Params &p, const Item &it, int m, int n, float v) {
     if (p.out_f32) {
         reinterpret_cast<float *>(it.y)[m * it.ldy + n] = v;
-    } else {
-        it.y[m * it.ldy + n] = f32_to_bf16_rn(v);
+        return;
     }
-}
-
-// The fused chain epilogue for one output whose BF16 value b is stored: the
-// next GEMM's input gets xn[m][k] = RNE_bf16(float(b) * scale) for every
-// k < xn_len with k = n (mod N) -- the elementwise step between the decode
-// chain's GEMMs, done on the value just rounded, so the result is bitwise that
-// of the separate step.
-__device__ __forceinline__ void store_next_input(const Params &p, const Item &it, int m, int n,
-                                                 uint16_t b) {
-    const uint16_t q = f32_to_bf16_rn(__uint_as_float(static_cast<uint32_t>(b) << 16) * p.xn_scale);
-    for (int k = n; k < p.xn_len; k += p.N) it.xn[m * it.ldxn + k] = q;
-}
-
-// The same for the rows of a warp's tasks in the streaming kernel, after its
-// main loop: task t covers rows [r0 + t * stride, + rows).  Out of line and
-// called once, so it does not touch the streaming loop's register allocation.
-static __device__ __noinline__ void warp_next_inputs(const uint16_t *y, long long ldy,
-                                                     uint16_t *xn, long long ldxn, int xn_len,
-                                                     int N, float scale, int M, int rows, int r0,
-                                                     int stride, int ntask, int lane) {
-    for (int t = 0; t < ntask; ++t) {
-        for (int i = lane; i < M * rows; i += 32) {
-            const int m = i / rows;
-            const int n = r0 + t * stride + (i - m * rows);
-            if (n >= N) continue;
-            const uint16_t b = y[m * ldy + n];
-            const uint16_t q = f32_to_bf16_rn(__uint_as_float(static_cast<uint32_t>(b) << 16) * scale);
-            for (int k = n; k < xn_len; k += N) xn[m * ldxn + k] = q;
-        }
-    }
-}
-
-// The same for the y rows [n0, n1) a CTA wrote, after its main loop: every
-// thread of the CTA calls it; the barrier makes the CTA's y stores visible to
-// all its threads, which then share the rows' next-input stores.
-__device__ __forceinline__ void store_next_inputs(const Params &p, const Item &it, int M, int n0,
-                                                  int n1) {
-    __syncthreads();
-    n1 = min(n1, p.N);
-    const int rows = n1 - n0;
-    for (int i = threadIdx.x; i < M * rows; i += blockDim.x) {
-        const int m = i / rows;
-        const int n = n0 + (i - m * rows);
-        store_next_input(p, it, m, n, it.y[m * it.ldy + n]);
+    const uint16_t b = f32_to_bf16_rn(v);
+    it.y[m * it.ldy + n] = b;
+    if (it.xn) {
+        const uint16_t q = f32_to_bf16_rn(__uint_as_float(static_cast<uint32_t>(b) << 16) * p.xn_scale);
+        for (int k = n; k < p.xn_len; k += p.N) it.xn[m * it.ldxn + k] = q;
     }
 }
 
@@ -519,14 +482,6 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
             if (base + U < total) issue_batch(bufA, base + U);
         }
     }
-
-    // fused chain epilogue: each warp re-reads the rows of its own tasks (written
-    // by lanes of this warp, visible after the warp barrier), no CTA barrier
-    if (it.xn && p.split == 1) {
-        __syncwarp();
-        warp_next_inputs(it.y, it.ldy, it.xn, it.ldxn, p.xn_len, p.N, p.xn_scale, M, G * R,
-                         g0 * G * R, warps * G * R, ntask, lane);
-    }
 }
 
 // Second pass of split-K: y = RNE_bf16(sum over splits, in split order).
@@ -550,7 +505,6 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
         for (int s = 0; s < p.split; ++s) acc += src[static_cast<long long>(s) * M * p.N];
         const Item &it = p.item[b];
         store_out(p, it, m, n, acc);
-        if (it.xn) store_next_input(p, it, m, n, f32_to_bf16_rn(acc));
     }
 }
 

@@ -179,8 +179,6 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mma_kernel(const __grid_co
             if (base + U < total) issue_batch(bA, base + U);
         }
     }
-    // fused chain epilogue: this CTA's rows are its tiles [t_begin, t_end)
-    if (it.xn && p.split == 1) store_next_inputs(p, it, M, t_begin * TILE, t_end * TILE);
 }
 
 }  // namespace sk

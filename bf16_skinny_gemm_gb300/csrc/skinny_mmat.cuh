@@ -163,8 +163,6 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mmat_kernel(const __grid_c
             if (base + U < total) issue_batch(wA, base + U);
         }
     }
-    // fused chain epilogue: this CTA's rows are its tiles [t_begin, t_end)
-    if (it.xn && p.split == 1) store_next_inputs(p, it, M, t_begin * TILE, t_end * TILE);
 }
 
 }  // namespace sk

@@ -165,13 +165,6 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mmatw_kernel(const __grid_
             if (base + U < total) issue_batch(wA, base + U);
         }
     }
-
-    // fused chain epilogue: this CTA's rows are the tiles of its groups
-    if (it.xn) {
-        const long long gg0 = static_cast<long long>(blockIdx.x) * groups;
-        store_next_inputs(p, it, M, static_cast<int>(T * gg0 / GG) * TILE,
-                          static_cast<int>(T * (gg0 + groups) / GG) * TILE);
-    }
 }
 
 }  // namespace sk
