@@ -184,3 +184,19 @@ def test_selected_plans_are_runnable(lib, N, K, M):
 def test_plan_select_out_of_range_still_returns_a_plan(lib):
     p = sk.sgemm_plan_select(-1, -1, 9)
     assert p.threads > 0 and p.id == -1
+
+
+def test_heuristic_plan_splits_k_when_rows_leave_sms_idle(lib):
+    # (288, 4096) at M = 1..4 has no table entry: 36 CTAs of rows alone would
+    # leave most of 152 SMs idle, so K is split (down to 512 elements a split)
+    for M in (1, 2, 3, 4):
+        p = sk.sgemm_plan_select(288, 4096, M)
+        assert p.id == -1 and p.split_k >= 4, p
+        assert sk.sgemm_plan_check(p, M, 288, 4096) == sk.SGEMM_OK
+    # enough rows: no extra split
+    assert sk.sgemm_plan_select(100000, 4096, 1).split_k == 1
+    # M >= 5 without a table entry: the 16-row tensor-core kernel
+    for M in (5, 8):
+        p = sk.sgemm_plan_select(3000, 2000, M)
+        assert p.id == -1 and p.variant == sk.SGEMM_VARIANT_MMA, p
+        assert sk.sgemm_plan_check(p, M, 3000, 2000) == sk.SGEMM_OK
