@@ -8,6 +8,7 @@ from __future__ import annotations
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -200,3 +201,19 @@ def test_heuristic_plan_splits_k_when_rows_leave_sms_idle(lib):
         p = sk.sgemm_plan_select(3000, 2000, M)
         assert p.id == -1 and p.variant == sk.SGEMM_VARIANT_MMA, p
         assert sk.sgemm_plan_check(p, M, 3000, 2000) == sk.SGEMM_OK
+
+
+def test_tensor_core_draft_compiles_for_sm103a(tmp_path):
+    """The TMA + tcgen05 kernel draft (csrc/skinny_tc05.cuh), not yet part of
+    the library, compiles for sm_103a: ptxas accepts its tensor-memory,
+    bulk-tensor and mbarrier instruction forms."""
+    src = tmp_path / "tc05.cu"
+    src.write_text('#include "skinny_tc05.cuh"\n'
+                   'const void *tc05_kernels[] = {\n'
+                   '    (const void *)&sk::tc05::skinny_tc05_kernel<1>,\n'
+                   '    (const void *)&sk::tc05::skinny_tc05_kernel<4>,\n'
+                   '    (const void *)&sk::tc05::skinny_tc05_kernel<8>};\n')
+    cmd = [skbuild.nvcc(), *skbuild.ARCH_FLAGS, "-O3", "-std=c++17", "-I", skbuild.CSRC,
+           "-I", skbuild.INCLUDE, "-c", str(src), "-o", str(tmp_path / "tc05.o")]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
