@@ -82,7 +82,9 @@ typedef struct {
     int lanes_per_row;    /* lanes sharing one row: 32, 16 or 8 (16/8 suit small K) */
     int k_unroll;         /* 16-byte W loads per row per lane kept in flight */
     int vec_bytes;        /* bytes per W load: 16 */
-    int split_k;          /* K split across this many CTAs (1 = none) */
+    int split_k;          /* K split across this many CTAs (1 = none); for
+                             SGEMM_VARIANT_MMA_TW, the warps of one CTA sharing each
+                             tile's K range (1, 2, 4 or 8), with no second pass */
     int stages;           /* pipeline depth: batches of loads in flight per warp, 1 or 2
                              (2 = double-buffered batches; 0 is read as 1) */
     int ctas_per_sm;      /* resident CTAs per SM the grid is sized for (0 = occupancy max) */
@@ -280,8 +282,10 @@ sgemm_status_t sgemm_bf16_rescale(const sgemm_bf16_t *y, long long n_src, sgemm_
  * SGEMM_NOALLOC_SCRATCH_BYTES (4 MiB) instead of allocated scratch.
  * - The caller passes inputs and outputs as for sgemm_bf16_skinny_ex (device
  *   pointers, strides in elements); split_k must be >= 2.  The selected plan
- *   is used with split_k splits; when the selected plan cannot split K (the
- *   bulk-copy variant), a CUDA-core streaming plan is used instead.
+ *   is used with split_k splits; when the selected plan cannot split K across
+ *   CTAs (the bulk-copy variant), a CUDA-core streaming plan is used instead,
+ *   and a warp-owned-tile plan (SGEMM_VARIANT_MMA_TW) runs as the x-as-A
+ *   tensor-core plan with the same unroll (SGEMM_VARIANT_MMA_T).
  * - split_k * M * N * 4 bytes must fit SGEMM_NOALLOC_SCRATCH_BYTES; larger
  *   problems return SGEMM_ERR_UNSUPPORTED_SHAPE and launch nothing.
  * - The first call on a device does a one-time set-up with that device current
