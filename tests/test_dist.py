@@ -1,6 +1,6 @@
 """Multi-process host logic of bench.py on CPU (gloo, world size 2).
 
-The skinny GEMM does not shard across GPUs in this build: bench.py runs one
+The skinny GEMM runs on one GPU per call: bench.py runs one
 independent replica per GPU (no collective on the data path).  What crosses
 ranks is only the timing protocol: a barrier around the timed region, the MAX
 of the elapsed times and the SUM of the bytes processed, and rank 0 alone
