@@ -227,8 +227,11 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
         mma_commit(saddr(bars + 2 * S));  // "done" once every issued MMA has completed
     }
 
-    // epilogue: every warp waits for "done", then reads its 32 rows x 16 columns
+    // epilogue: every warp waits for "done", then reads its 32 rows x 16 columns.
+    // tcgen05.ld is warp-wide: the warp reconverges first (lane 0 of warps 0 and 1
+    // comes from its own loop, and each lane leaves the bounded wait on its own).
     bool done_ok = bar_wait(saddr(bars + 2 * S), 0);
+    __syncwarp();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     uint32_t r[16];
     asm volatile(
