@@ -68,7 +68,17 @@ def candidates(M, N, K, splits):
     return out
 
 
-def sweep_shape(N, K, Ms, splits, flags, trials, replays, min_bytes, pair=False, log=print):
+def sweep_shape(N, K, Ms, splits, flags, trials, replays, min_bytes, pair=False, log=print,
+                prefilter=0, prefilter_bytes=0.0):
+    """Time every candidate plan of (N, K) for each M; returns {M: result}.
+
+    prefilter = P > 0 times the candidates in two stages: first all of them on
+    a shorter chain (weight copies totalling ``prefilter_bytes``, still at least
+    twice L2 so every GEMM reads HBM) with 2 trials x 5 replays, then the P
+    fastest (and the heuristic plan) with the full protocol; the winner comes
+    from the second stage.  This cuts the graph captures that dominate the
+    sweep's time for small weights.
+    """
     dev = torch.device("cuda")
     R = max(2, math.ceil(min_bytes / (2 * N * K)))
     if pair:
@@ -78,58 +88,76 @@ def sweep_shape(N, K, Ms, splits, flags, trials, replays, min_bytes, pair=False,
     for i in range(R):
         W[i].copy_(synth.normal_bf16((N, K), std, seed=i, device=dev))
     results = {}
+
+    def same(a, b):
+        da, db = a.as_dict(), b.as_dict()
+        da.pop("id"), db.pop("id")
+        return da == db
+
     for M in Ms:
         x = synth.normal_bf16((R, M, K), synth.X_STD, seed=1000 + M, device=dev)
         y = torch.empty((R, M, N), dtype=torch.bfloat16, device=dev)
         cands = candidates(M, N, K, splits)
         heur = sk.sgemm_plan_select(N, K, M)
-        graphs = []
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
 
-        def chain(plan, fl):
+        def chain(plan, fl, n):
             if pair:
-                for i in range(0, R, 2):
+                for i in range(0, n, 2):
                     sk.sgemm_bf16_skinny_batched_ex([(x[i], W[i], y[i]), (x[i + 1], W[i + 1], y[i + 1])],
                                                     plan=plan, flags=fl)
             else:
-                for i in range(R):
+                for i in range(n):
                     sk.sgemm_bf16_skinny_ex(x[i], W[i], y[i], plan=plan, flags=fl)
 
-        for p in cands:
-            chain(p, 0)  # eager once (split-K scratch is allocated outside capture)
-        torch.cuda.synchronize()
-        for p in cands:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(s):
-                with torch.cuda.graph(g, stream=s):
-                    chain(p, flags)
-            graphs.append(g)
-        torch.cuda.current_stream().wait_stream(s)
-        for g in graphs:
-            g.replay()
-            g.replay()
-        torch.cuda.synchronize()
-        times = [[] for _ in cands]
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        for _ in range(trials):
-            for ci, g in enumerate(graphs):
-                e0.record()
-                for _ in range(replays):
-                    g.replay()
-                e1.record()
-                e1.synchronize()
-                per_launch = R // 2 if pair else R
-                times[ci].append(e0.elapsed_time(e1) * 1e3 / replays / per_launch)
-        med = [statistics.median(t) for t in times]
+        def time_plans(plans, n, n_trials, n_replays):
+            """Median µs per launch of each plan over a graph of n GEMMs."""
+            for p in plans:
+                chain(p, 0, n)  # eager once (split-K scratch is allocated outside capture)
+            torch.cuda.synchronize()
+            graphs = []
+            for p in plans:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(s):
+                    with torch.cuda.graph(g, stream=s):
+                        chain(p, flags, n)
+                graphs.append(g)
+            torch.cuda.current_stream().wait_stream(s)
+            for g in graphs:
+                g.replay()
+                g.replay()
+            torch.cuda.synchronize()
+            times = [[] for _ in plans]
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            per_launch = n // 2 if pair else n
+            for _ in range(n_trials):
+                for ci, g in enumerate(graphs):
+                    e0.record()
+                    for _ in range(n_replays):
+                        g.replay()
+                    e1.record()
+                    e1.synchronize()
+                    times[ci].append(e0.elapsed_time(e1) * 1e3 / n_replays / per_launch)
+            del graphs
+            torch.cuda.synchronize()
+            return [statistics.median(t) for t in times]
+
+        stage1 = None
+        if prefilter > 0 and len(cands) > prefilter:
+            R1 = min(R, max(2, math.ceil(prefilter_bytes / (2 * N * K))))
+            R1 += R1 % 2 if pair else 0
+            med1 = time_plans(cands, R1, 2, 5)
+            keep = sorted(range(len(cands)), key=lambda i: med1[i])[:prefilter]
+            keep += [i for i, p in enumerate(cands) if same(p, heur) and i not in keep]
+            stage1 = [(cands[i].as_dict(), round(med1[i], 3)) for i in
+                      sorted(range(len(cands)), key=lambda i: med1[i])]
+            cands = [cands[i] for i in keep]
+        med = time_plans(cands, R, trials, replays)
         order = sorted(range(len(cands)), key=lambda i: med[i])
         best = cands[order[0]]
         nbytes = (2 if pair else 1) * 2 * (N * K + M * K + M * N)
-        def same(a, b):
-            da, db = a.as_dict(), b.as_dict()
-            da.pop("id"), db.pop("id")
-            return da == db
         heur_us = next((med[i] for i, p in enumerate(cands) if same(p, heur)), None)
         results[M] = {"plan": best.as_dict(), "us": med[order[0]],
                       "gbs": nbytes / med[order[0]] / 1e3,
@@ -137,11 +165,12 @@ def sweep_shape(N, K, Ms, splits, flags, trials, replays, min_bytes, pair=False,
                       "top": [(cands[i].as_dict(), round(med[i], 3)) for i in order[:5]],
                       "all": [(cands[i].as_dict(), round(med[i], 3)) for i in order],
                       "copies": R, "candidates": len(cands)}
+        if stage1 is not None:
+            results[M]["prefilter"] = stage1
         log(f"  N={N} K={K} M={M}: best {med[order[0]]:.3f} us "
             f"({results[M]['gbs']:.0f} GB/s) {_short(best)}; heuristic "
-            f"{heur_us if heur_us is None else round(heur_us, 3)} us; {len(cands)} candidates")
-        del graphs
-        torch.cuda.synchronize()
+            f"{heur_us if heur_us is None else round(heur_us, 3)} us; {len(cands)} candidates"
+            + ("" if stage1 is None else f" (of {len(stage1)} prefiltered)"))
     del W
     torch.cuda.empty_cache()
     return results
@@ -203,6 +232,9 @@ def main(argv=None):
     ap.add_argument("--no-pair", action="store_true")
     ap.add_argument("--merge", default=None,
                     help="start from this existing table and replace only the swept entries")
+    ap.add_argument("--prefilter", type=int, default=0,
+                    help="time all candidates on a shorter cold chain first and keep this many "
+                         "for the full protocol (0 = time every candidate fully)")
     args = ap.parse_args(argv)
 
     assert torch.cuda.is_available(), "the sweep runs on the GPU"
@@ -221,19 +253,23 @@ def main(argv=None):
     if args.merge:
         entries = read_table(args.merge)
     for (N, K) in shapes:
-        res = sweep_shape(N, K, Ms, splits, flags, args.trials, args.replays, min_bytes)
+        res = sweep_shape(N, K, Ms, splits, flags, args.trials, args.replays, min_bytes,
+                          prefilter=args.prefilter, prefilter_bytes=2 * l2)
         for M, r in res.items():
             entries[(N, K, M)] = r
             dump[f"{N}x{K}x{M}"] = r
     if not args.no_pair:
         N, K = PAIR_SHAPE
-        res = sweep_shape(N, K, Ms, splits, flags, args.trials, args.replays, min_bytes, pair=True)
+        res = sweep_shape(N, K, Ms, splits, flags, args.trials, args.replays, min_bytes, pair=True,
+                          prefilter=args.prefilter, prefilter_bytes=2 * l2)
         for M, r in res.items():
             entries[(N, K, M)] = r
             dump[f"{N}x{K}x{M}-pair"] = r
     note = (f"{torch.cuda.get_device_name(0)}, {len(entries)} entries, cold L2 (>= "
             f"{min_bytes / 2**30:.2f} GiB of weight copies per shape), launch flags PDL|readonly, "
-            f"{args.trials} interleaved trials x {args.replays} graph replays, median")
+            f"{args.trials} interleaved trials x {args.replays} graph replays, median"
+            + (f", top {args.prefilter} of a shorter cold chain (>= 2 x L2) timed fully"
+               if args.prefilter else ""))
     write_table(entries, args.out, note)
     if args.json:
         with open(args.json, "w") as f:

@@ -217,3 +217,22 @@ def test_tensor_core_draft_compiles_for_sm103a(tmp_path):
            "-I", skbuild.INCLUDE, "-c", str(src), "-o", str(tmp_path / "tc05.o")]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+def test_plan_table_round_trip(tmp_path):
+    """The sweep's table writer and reader (used by --merge) agree, and the
+    compiled table parses: every entry is a plan the library accepts."""
+    from bf16_skinny_gemm_gb300 import sweep
+    entries = sweep.read_table(os.path.join(skbuild.CSRC, "plan_table.inc"))
+    assert len(entries) >= 32
+    for (N, K, M), r in entries.items():
+        plan = sk.Plan(**{**r["plan"], "id": -1})
+        assert sk.sgemm_plan_check(plan, M, N, K) == sk.SGEMM_OK, (N, K, M, r["plan"])
+        assert sk.sgemm_plan_select(N, K, M).id >= 0, (N, K, M)
+    out = tmp_path / "table.inc"
+    sweep.write_table(entries, str(out), "round trip")
+    again = sweep.read_table(str(out))
+    assert again.keys() == entries.keys()
+    for k in entries:
+        assert again[k]["plan"] == entries[k]["plan"]
+        assert abs(again[k]["us"] - entries[k]["us"]) < 1e-3
