@@ -3,9 +3,10 @@
 //     y[M,N] = x[M,K] . W[N,K]^T,   M <= 16,   BF16 in, FP32 accumulation
 //
 // STATUS: compiled for sm_103a by the CPU test-suite (tests/test_abi.py), so
-// ptxas checks every instruction form below; not yet part of the library (no
-// translation unit of it includes this file) and never run on a GPU.  It
-// becomes a plan variant only after parity tests against the oracle pass.
+// ptxas checks every instruction form below and the host launch compiles; not
+// yet part of the library (no translation unit of it includes this file) and
+// never run on a GPU.  It becomes a plan variant only after parity tests
+// against the oracle pass.
 //
 // Why: the mma.sync kernels of this library load W through registers in the
 // fragment layout (8 rows x 64 bytes per warp instruction) and stop at 0.66 to
@@ -322,6 +323,55 @@ inline cudaError_t encode_maps(Tc05Params &p, const uint16_t *x, long long ldx, 
             return cudaErrorInvalidValue;
     }
     return cudaSuccess;
+}
+
+// Host: one launch of the kernel for y = x . W^T (one problem), M <= 16.
+// grid = (ceil(N / 128) tiles, split); split > 1 writes FP32 partials to ws
+// ([split][M][N], caller-provided) for the library's split-K second pass,
+// which the caller launches after this.  kps (K per split) is rounded up to
+// whole 64-element stages, so the splits actually used (stored in *split_used
+// when given; the second pass must use that count) may be fewer than asked.
+// Flags as Params::flags (PDL launch attribute when kFlagPdl is set).  Returns
+// the launch's CUDA status.
+template <int M>
+inline cudaError_t launch(const uint16_t *x, long long ldx, const uint16_t *W, uint16_t *y,
+                          long long ldy, int N, int K, int split, int stages, float *ws,
+                          int *err, int flags, cudaStream_t stream, int *split_used = nullptr) {
+    Tc05Params p;
+    cudaError_t e = encode_maps(p, x, ldx, W, M, N, K);
+    if (e != cudaSuccess) return e;
+    const int nst = (K + kBoxK - 1) / kBoxK;
+    const int per = (nst + split - 1) / split;
+    p.y = y;
+    p.ldy = ldy;
+    p.ws = ws;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.kps = per * kBoxK;
+    p.split = (nst + per - 1) / per;  // every split non-empty
+    if (split_used) *split_used = p.split;
+    p.stages = stages;
+    p.flags = flags;
+    p.err = err;
+    const size_t smem = smem_bytes(stages);
+    e = cudaFuncSetAttribute(skinny_tc05_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((N + kRows - 1) / kRows),
+                       static_cast<unsigned>(p.split), 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (flags & kFlagPdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, skinny_tc05_kernel<M>, p);
 }
 
 }  // namespace tc05

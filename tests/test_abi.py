@@ -212,7 +212,11 @@ def test_tensor_core_draft_compiles_for_sm103a(tmp_path):
                    'const void *tc05_kernels[] = {\n'
                    '    (const void *)&sk::tc05::skinny_tc05_kernel<1>,\n'
                    '    (const void *)&sk::tc05::skinny_tc05_kernel<4>,\n'
-                   '    (const void *)&sk::tc05::skinny_tc05_kernel<8>};\n')
+                   '    (const void *)&sk::tc05::skinny_tc05_kernel<8>};\n'
+                   'cudaError_t tc05_launch_m4(const uint16_t *x, const uint16_t *W, uint16_t *y,\n'
+                   '                           int N, int K, cudaStream_t s) {\n'
+                   '    return sk::tc05::launch<4>(x, K, W, y, N, N, K, 1, 4, nullptr, nullptr, 0, s);\n'
+                   '}\n')
     cmd = [skbuild.nvcc(), *skbuild.ARCH_FLAGS, "-O3", "-std=c++17", "-I", skbuild.CSRC,
            "-I", skbuild.INCLUDE, "-c", str(src), "-o", str(tmp_path / "tc05.o")]
     r = subprocess.run(cmd, capture_output=True, text=True)
