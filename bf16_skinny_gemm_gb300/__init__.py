@@ -28,7 +28,8 @@ __all__ = [
     "SGEMM_OK", "SGEMM_ERR_INVALID_ARG", "SGEMM_ERR_UNSUPPORTED_SHAPE", "SGEMM_ERR_MISALIGNED",
     "SGEMM_ERR_UNSUPPORTED_DEVICE", "SGEMM_ERR_NO_WORKSPACE", "SGEMM_ERR_CUDA", "MAX_BATCH",
     "SGEMM_VARIANT_LDG", "SGEMM_VARIANT_LDG_MIXFMA", "SGEMM_VARIANT_MMA", "SGEMM_VARIANT_MMA_T", "SGEMM_VARIANT_BULK", "SGEMM_VARIANT_LDG_FFMA2", "SGEMM_VARIANT_LDGX_MIXFMA",
-    "SGEMM_VARIANT_LDGX_FFMA2", "SGEMM_VARIANT_MMA_TW", "SGEMM_VARIANT_LDG_MMA", "SGEMM_FLAG_PDL",
+    "SGEMM_VARIANT_LDGX_FFMA2", "SGEMM_VARIANT_MMA_TW", "SGEMM_VARIANT_LDG_MMA",
+    "SGEMM_VARIANT_TC05", "SGEMM_FLAG_PDL",
     "SGEMM_FLAG_TEST_STALL", "sgemm_device_errors",
     "SGEMM_FLAG_WEIGHTS_READONLY",
 ]
@@ -51,6 +52,7 @@ SGEMM_VARIANT_LDGX_MIXFMA = 6
 SGEMM_VARIANT_LDGX_FFMA2 = 7
 SGEMM_VARIANT_MMA_TW = 8
 SGEMM_VARIANT_LDG_MMA = 9
+SGEMM_VARIANT_TC05 = 10
 SGEMM_FLAG_TEST_STALL = 4
 SGEMM_FLAG_PDL = 1
 SGEMM_FLAG_WEIGHTS_READONLY = 2
@@ -369,7 +371,7 @@ def sgemm_init() -> None:
 
 def sgemm_device_errors() -> int:
     """Read and clear the device error word of the current device (synchronous).
-    Bit 0: a bulk-copy kernel gave up waiting for its data and wrote NaN."""
+    Bit 0: a kernel gave up a bounded wait for its data and wrote NaN outputs."""
     v = ctypes.c_int(0)
     _check(load().sgemm_device_errors(ctypes.byref(v)), "sgemm_device_errors")
     return v.value

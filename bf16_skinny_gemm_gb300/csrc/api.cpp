@@ -17,6 +17,7 @@
 #include <vector>
 
 #include "internal.h"
+#include "tc05_consts.h"
 
 namespace {
 
@@ -57,7 +58,8 @@ const KernelInfo *table_for_m(int M) {
 const KernelInfo *find_kernel(int variant, int M, int R, int LPR, int U, int stages) {
     const KernelInfo *t = table_for_m(M);
     if (!t) return nullptr;
-    if (variant == SGEMM_VARIANT_BULK) {  // one kernel per M; the rest are launch parameters
+    if (variant == SGEMM_VARIANT_BULK || variant == SGEMM_VARIANT_TC05) {
+        // one kernel per M; the rest are launch parameters
         for (int i = 0; i < sk::kKernelCountPerM; ++i)
             if (t[i].variant == variant && t[i].R == R && t[i].LPR == LPR) return &t[i];
         return nullptr;
@@ -74,6 +76,7 @@ struct DeviceState {
     bool probed = false;
     bool supported = false;
     int sms = 0;
+    int *err = nullptr;  // device error word (a static device variable of the library)
     float *ws = nullptr;
     size_t ws_bytes = 0;
     std::map<std::tuple<const void *, int, size_t>, int> occupancy;
@@ -98,9 +101,28 @@ sgemm_status_t check_bulk_plan(const sgemm_plan_t &p, int M, int K) {
     return SGEMM_OK;
 }
 
+sgemm_status_t check_tc05_plan(const sgemm_plan_t &p, int M, int K) {
+    if (p.threads != sk::tc05::kThreads || p.rows_per_warp != sk::tc05::kRows ||
+        p.lanes_per_row != 0 || p.vec_bytes != 16)
+        return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (p.k_unroll != 1 && p.k_unroll != 2 && p.k_unroll != 4) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (p.stages < 2 || p.stages > sk::tc05::kMaxRingSlots) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (p.ctas_per_sm < 0 || p.ctas_per_sm > 8) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    const int kbox = (K + sk::tc05::kBoxK - 1) / sk::tc05::kBoxK;
+    if (p.split_k < 1 || p.split_k > sk::tc05::kMaxSplit || p.split_k > kbox)
+        return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (!find_kernel(p.variant, M, p.rows_per_warp, p.lanes_per_row, 0, 0))
+        return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    // leave 1 KiB for the kernel's static shared memory (mbarriers, flags)
+    const size_t smem = sk::tc05_smem_bytes(M, p.stages, p.k_unroll, sk::tc05_splits_used(K, p.split_k));
+    if (smem + 1024 > kMaxSmem) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    return SGEMM_OK;
+}
+
 sgemm_status_t check_plan(const sgemm_plan_t &p, int M, int N, int K) {
     (void)N;
     if (p.variant == SGEMM_VARIANT_BULK) return check_bulk_plan(p, M, K);
+    if (p.variant == SGEMM_VARIANT_TC05) return check_tc05_plan(p, M, K);
     if (p.variant != SGEMM_VARIANT_LDG && p.variant != SGEMM_VARIANT_LDG_MIXFMA &&
         p.variant != SGEMM_VARIANT_LDG_FFMA2 && p.variant != SGEMM_VARIANT_MMA &&
         p.variant != SGEMM_VARIANT_MMA_T && p.variant != SGEMM_VARIANT_LDGX_MIXFMA &&
@@ -151,6 +173,28 @@ sgemm_plan_t make_plan(int variant, int threads, int R, int LPR, int U, int spli
 // when the x slice would not leave room for two CTAs per SM, and further while
 // the rows alone give fewer than two CTAs per SM of a GB300 (152 SMs) and each
 // split keeps at least 512 elements of K.
+// SM count of the current device (cached per device); 152, a GB300's count,
+// when no device can be queried (plan selection is a host function).
+int current_sm_count() {
+    static std::mutex mu;
+    static std::map<int, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 152;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
+        (void)cudaGetLastError();
+        sms = 152;
+    }
+    cache[dev] = sms;
+    return sms;
+}
+
 sgemm_plan_t heuristic_plan(int N, int K, int M) {
     int variant = SGEMM_VARIANT_LDG_MIXFMA;
     int R, LPR, U, rows_per_cta;
@@ -175,7 +219,8 @@ sgemm_plan_t heuristic_plan(int N, int K, int M) {
         split = static_cast<int>((xbytes + budget - 1) / budget);
         split = std::max(1, std::min(split, 64));
         const long long ctas = (static_cast<long long>(std::max(N, 1)) + rows_per_cta - 1) / rows_per_cta;
-        while (split < 16 && ctas * split < 2 * 152 && K / (2 * split) >= 512) split *= 2;
+        const long long sms = current_sm_count();
+        while (split < 16 && ctas * split < 2 * sms && K / (2 * split) >= 512) split *= 2;
     }
     return make_plan(variant, 256, R, LPR, U, split, 1, 0, -1);
 }
@@ -191,9 +236,10 @@ sgemm_status_t probe_device(int *dev_out, DeviceState **st_out) {
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return SGEMM_ERR_CUDA;
-        st.probed = true;
         st.supported = (major == 10 && minor == 3);
         st.sms = sms;
+        if (st.supported && sk::device_error_word(&st.err) != cudaSuccess) return SGEMM_ERR_CUDA;
+        st.probed = true;
     }
     if (!st.supported) return SGEMM_ERR_UNSUPPORTED_DEVICE;
     *dev_out = dev;
@@ -201,12 +247,8 @@ sgemm_status_t probe_device(int *dev_out, DeviceState **st_out) {
     return SGEMM_OK;
 }
 
-// The last kErrBytes of the scratch hold the device error word of the bulk kernel.
-constexpr size_t kErrBytes = 256;
-
-// Requires g_mu held.  `bytes` is the partial-sum space needed before the error word.
+// Requires g_mu held.  `bytes` is the partial-sum space needed.
 sgemm_status_t ensure_workspace(DeviceState &st, size_t bytes, cudaStream_t stream) {
-    bytes += kErrBytes;
     if (st.ws && st.ws_bytes >= bytes) return SGEMM_OK;
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return SGEMM_ERR_NO_WORKSPACE;
@@ -221,17 +263,9 @@ sgemm_status_t ensure_workspace(DeviceState &st, size_t bytes, cudaStream_t stre
     }
     void *p = nullptr;
     if (cudaMalloc(&p, want) != cudaSuccess) return SGEMM_ERR_CUDA;
-    if (cudaMemset(static_cast<char *>(p) + want - kErrBytes, 0, kErrBytes) != cudaSuccess) {
-        cudaFree(p);
-        return SGEMM_ERR_CUDA;
-    }
     st.ws = static_cast<float *>(p);
     st.ws_bytes = want;
     return SGEMM_OK;
-}
-
-int *error_word(DeviceState &st) {
-    return reinterpret_cast<int *>(reinterpret_cast<char *>(st.ws) + st.ws_bytes - kErrBytes);
 }
 
 // Requires g_mu held.
@@ -296,6 +330,53 @@ sgemm_status_t validate_epilogue(const Epilogue &ep, const sgemm_pair_t &it, int
     return SGEMM_OK;
 }
 
+// The common kernel parameters of one launch (no split-K scratch).
+sk::Params make_params(const sgemm_pair_t *items, int batch, int N, int K, unsigned flags,
+                       const Epilogue &ep) {
+    sk::Params prm;
+    std::memset(&prm, 0, sizeof(prm));
+    for (int b = 0; b < batch; ++b) {
+        prm.item[b].x = items[b].x;
+        prm.item[b].W = items[b].W;
+        prm.item[b].y = items[b].y;
+        prm.item[b].ldx = items[b].ldx;
+        prm.item[b].ldy = items[b].ldy;
+        prm.item[b].xn = ep.xn;
+        prm.item[b].ldxn = ep.ldxn;
+    }
+    prm.out_f32 = ep.out_f32 ? 1 : 0;
+    prm.xn_len = static_cast<int>(ep.xn_len);
+    prm.xn_scale = ep.xn_scale;
+    prm.N = N;
+    prm.K = K;
+    prm.split = 1;
+    prm.flags = static_cast<int>(flags);
+    return prm;
+}
+
+// The TMA + tcgen05 kernel: one launch, no scratch (its K split reduces inside
+// a thread-block cluster).
+sgemm_status_t run_tc05(const sgemm_pair_t *items, int batch, int M, int N, int K,
+                        const sgemm_plan_t &plan, unsigned flags, cudaStream_t stream,
+                        const Epilogue &ep, DeviceState &st, const void *fn) {
+    sk::Params prm = make_params(items, batch, N, K, flags, ep);
+    prm.err = st.err;
+    long long ctas = 1;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!st.smem_attr_set[fn]) {
+            if (sk::allow_max_dynamic_smem(fn) != cudaSuccess) return SGEMM_ERR_CUDA;
+            st.smem_attr_set[fn] = true;
+        }
+        const size_t smem = sk::tc05_smem_bytes(M, plan.stages, plan.k_unroll, 1);
+        const int occ = plan.ctas_per_sm > 0 ? plan.ctas_per_sm
+                                             : occupancy(st, fn, sk::tc05::kThreads, smem);
+        ctas = std::max<long long>(1, static_cast<long long>(st.sms) * occ / batch);
+    }
+    if (sk::tc05_launch(prm, batch, M, plan, ctas, fn, stream) != cudaSuccess) return SGEMM_ERR_CUDA;
+    return SGEMM_OK;
+}
+
 sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
                    const sgemm_plan_t *plan_in, unsigned flags, cudaStream_t stream,
                    const Epilogue &ep = Epilogue()) {
@@ -322,6 +403,8 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
 
     const KernelInfo *ki = find_kernel(plan.variant, M, plan.rows_per_warp, plan.lanes_per_row,
                                        plan.k_unroll, plan.stages);
+    if (plan.variant == SGEMM_VARIANT_TC05) return run_tc05(items, batch, M, N, K, plan, flags,
+                                                            stream, ep, *st, ki->fn);
     const bool bulk = plan.variant == SGEMM_VARIANT_BULK;
     const bool tw = plan.variant == SGEMM_VARIANT_MMA_TW;  // split_k splits K inside a CTA
     const int split = tw ? 1 : plan.split_k;
@@ -359,11 +442,7 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
             if (s != SGEMM_OK) return s;
             prm.ws = st->ws;
         }
-        if (bulk) {
-            s = ensure_workspace(*st, 0, stream);
-            if (s != SGEMM_OK) return s;
-            prm.err = error_word(*st);
-        }
+        prm.err = st->err;
         if (!st->smem_attr_set[ki->fn]) {
             if (sk::allow_max_dynamic_smem(ki->fn) != cudaSuccess) return SGEMM_ERR_CUDA;
             st->smem_attr_set[ki->fn] = true;
@@ -454,6 +533,7 @@ size_t smem_bytes(const sgemm_plan_t &plan, int M, int kps) {
 }
 
 int work_units(const sgemm_plan_t &plan, int N) {
+    if (plan.variant == SGEMM_VARIANT_TC05) return (N + tc05::kRows - 1) / tc05::kRows;
     if (plan.variant == SGEMM_VARIANT_MMA) return (N + 15) / 16;
     if (plan.variant == SGEMM_VARIANT_MMA_T || plan.variant == SGEMM_VARIANT_BULK ||
         plan.variant == SGEMM_VARIANT_MMA_TW)
@@ -473,7 +553,7 @@ cudaError_t allow_max_dynamic_smem(const void *fn) {
 long long ctas_wanted(const sgemm_plan_t &plan, int N) {
     const long long units = work_units(plan, N);
     if (plan.variant == SGEMM_VARIANT_MMA || plan.variant == SGEMM_VARIANT_MMA_T ||
-        plan.variant == SGEMM_VARIANT_BULK)
+        plan.variant == SGEMM_VARIANT_BULK || plan.variant == SGEMM_VARIANT_TC05)
         return units;  // one tile per CTA at most
     if (plan.variant == SGEMM_VARIANT_MMA_TW) {
         const int groups = std::max(1, plan.threads / 32 / std::max(1, plan.split_k));
@@ -508,6 +588,13 @@ sgemm_status_t sgemm_plan_get(int index, sgemm_plan_t *plan) {
         // producer warp + 8 or 4 consumer warps; 1024-wide stages, 4 ring slots
         const int threads = (index % kNumThreadChoices) == 0 ? 288 : 160;
         *plan = make_plan(k.variant, threads, 8, 4, 32, 1, 4, 0, -1);
+        return SGEMM_OK;
+    }
+    if (k.variant == SGEMM_VARIANT_TC05) {
+        // six single-box stages, or three stages of two boxes (the same bytes in flight)
+        const bool first = (index % kNumThreadChoices) == 0;
+        *plan = make_plan(k.variant, sk::tc05::kThreads, sk::tc05::kRows, 0, first ? 1 : 2, 1,
+                          first ? 6 : 3, 0, -1);
         return SGEMM_OK;
     }
     *plan = make_plan(k.variant, kThreadChoices[index % kNumThreadChoices], k.R, k.LPR, k.U, 1,
@@ -604,9 +691,8 @@ sgemm_status_t sgemm_device_errors(int *flags) {
     sgemm_status_t s = probe_device(&dev, &st);
     if (s != SGEMM_OK) return s;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!st->ws) return SGEMM_OK;
     if (cudaDeviceSynchronize() != cudaSuccess) return SGEMM_ERR_CUDA;
-    int *w = error_word(*st);
+    int *w = st->err;
     if (cudaMemcpy(flags, w, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
         cudaMemset(w, 0, sizeof(int)) != cudaSuccess)
         return SGEMM_ERR_CUDA;

@@ -2,6 +2,7 @@
 // units of the BF16 skinny GEMM (y[M,N] = x[M,K] . W[N,K]^T, M <= 8).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -48,6 +49,21 @@ struct Params {
     int out_f32;     // 1: y holds FP32 outputs (no BF16 rounding)
     int xn_len;      // fused chain epilogue: xn[m][k] for 0 <= k < xn_len ...
     float xn_scale;  // ... = RNE_bf16(float(y[m][k mod N]) * xn_scale)
+};
+
+// Kernel parameters of the TMA + tcgen05 kernel (skinny_tc05.cuh): the common
+// parameters plus one pair of tensor maps (W and x) per problem, which the
+// copy engine reads from the kernel's parameter space.  About 2.6 KB.
+struct alignas(64) Tc05Params {
+    CUtensorMap tw[kMaxBatch];  // W [N][K]: dims {K, N}, box {64, 128}, 128-byte swizzle
+    CUtensorMap tx[kMaxBatch];  // x [M][K] (row stride ldx): dims {K, M}, box {64, 16}
+    Params base;                // y, strides, epilogue, flags, error word (ws unused)
+    int tiles;                  // ceil(N / 128)
+    int kbox;                   // ceil(K / 64): 64-element boxes along K
+    int per;                    // boxes per K split
+    int split;                  // CTAs per cluster sharing a tile (1 = persistent grid)
+    int ring;                   // shared-memory stages
+    int nb;                     // boxes per stage
 };
 
 #ifdef __CUDACC__
@@ -111,5 +127,23 @@ int work_units(const sgemm_plan_t &plan, int N);
 long long ctas_wanted(const sgemm_plan_t &plan, int N);
 // Let a kernel use all the dynamic shared memory its static part leaves.
 cudaError_t allow_max_dynamic_smem(const void *fn);
+
+// The device error word of the current device (a static device variable of
+// the library; bit 0: a kernel gave up a bounded wait).  Defined in
+// tc05_launch.cu, which owns the variable.
+cudaError_t device_error_word(int **out);
+
+// The TMA + tcgen05 kernel (defined in tc05_launch.cu).  K boxes per split and
+// the splits actually used for K and `split` CTAs requested: every split
+// non-empty, so fewer may be used.
+int tc05_boxes_per_split(int K, int split);
+int tc05_splits_used(int K, int split);
+// Dynamic shared memory of one CTA.
+size_t tc05_smem_bytes(int M, int ring, int nb, int splits_used);
+// Launch y = x . W^T for the problems in `base` (batch of them, all (M, N, K))
+// with this plan; `fn` is the kernel for M, `ctas` the persistent grid's CTAs
+// per problem when the plan does not split K.  Returns the CUDA status.
+cudaError_t tc05_launch(const Params &base, int batch, int M, const sgemm_plan_t &plan,
+                        long long ctas, const void *fn, cudaStream_t stream);
 
 }  // namespace sk

@@ -12,6 +12,7 @@
 #include "skinny_mmat.cuh"
 #include "skinny_bulk.cuh"
 #include "skinny_mmatw.cuh"
+#include "skinny_tc05.cuh"
 
 #define SK_LDG_CONFIGS(X, M)   \
     X(M, 1, 32, 8, 0, false)   \
@@ -113,8 +114,15 @@
 #define SK_BULK_ENTRY(M) \
     {SGEMM_VARIANT_BULK, M, 8, 4, 0, 0, reinterpret_cast<const void *>(&skinny_bulk_kernel<M>)},
 
+// TMA + tcgen05 kernel: one instantiation per M; tile rows 128, and the ring
+// depth, boxes per stage and cluster split are launch parameters (U = 0,
+// stages = 0 mark "any").
+#define SK_TC05_ENTRY(M) \
+    {SGEMM_VARIANT_TC05, M, 128, 0, 0, 0, reinterpret_cast<const void *>(&tc05::skinny_tc05_kernel<M>)},
+
 #define SK_DEFINE_TABLE(M, NAME)                                                          \
     const KernelInfo NAME[] = {SK_LDG_CONFIGS(SK_LDG_ENTRY, M) SK_MMA_CONFIGS(SK_MMA_ENTRY, M) \
                                    SK_MMAT_CONFIGS(SK_MMAT_ENTRY, M) SK_BULK_ENTRY(M)     \
                                        SK_LDGX_CONFIGS(SK_LDGX_ENTRY, M)   \
-                                           SK_MMATW_CONFIGS(SK_MMATW_ENTRY, M)};
+                                           SK_MMATW_CONFIGS(SK_MMATW_ENTRY, M) \
+                                               SK_TC05_ENTRY(M)};

@@ -1,83 +1,74 @@
-// Tensor-core skinny GEMM on the Blackwell data path (sm_103a) -- a draft.
+// Tensor-core skinny GEMM on the Blackwell data path (sm_103a):
 //
-//     y[M,N] = x[M,K] . W[N,K]^T,   M <= 16,   BF16 in, FP32 accumulation
+//     y[M,N] = x[M,K] . W[N,K]^T,   M <= 8,   BF16 in, FP32 accumulation
 //
-// STATUS: compiled for sm_103a by the CPU test-suite (tests/test_abi.py), so
-// ptxas checks every instruction form below and the host launch compiles; not
-// yet part of the library (no translation unit of it includes this file) and
-// never run on a GPU.  It becomes a plan variant only after parity tests
-// against the oracle pass.
+// The operation is the decode projection of vLLM PR #62949 ("SM121 skinny-GEMM
+// plans for the GLM-5.3-Flash BF16 decode projections", Validation: each
+// weight is read once per step) and PR #65306 ("Add SM90 skinny GEMM plans
+// ...", Details: a library GEMM spends a split-K reduce kernel on these
+// shapes).  This kernel is our own design for GB300:
 //
-// Why: the mma.sync kernels of this library load W through registers in the
-// fragment layout (8 rows x 64 bytes per warp instruction) and stop at 0.66 to
-// 0.73 of the HBM peak for M = 4..8, while a library GEMM reaches about 0.8 at
-// M = 8 on the same shapes.  Here W never passes through registers:
-//  * a producer thread streams boxes of 128 rows x 64 elements of W (16 KiB)
-//    and the matching 16 x 64 box of x (2 KiB; rows >= M and columns >= K are
-//    zero-filled by the copy engine) with cp.async.bulk.tensor into a ring of
-//    S shared-memory stages, 128-byte swizzled; each stage completes on its
-//    "full" mbarrier;
-//  * an MMA thread issues, per stage, four tcgen05.mma.kind::f16 of
-//    M = 128 (rows of W) x N = 16 (rows of x) x K = 16, both operands K-major
-//    in shared memory (128-byte-swizzle descriptors, advanced 32 bytes per K
-//    step), FP32 accumulator in tensor memory, then tcgen05.commit onto the
-//    stage's "empty" mbarrier, which hands the stage back to the producer;
-//    after the last stage a commit onto "done";
-//  * four warps read the 128 x 16 accumulator with tcgen05.ld (warp w owns
-//    tensor-memory lanes 32w .. 32w+31, the tile's rows) and store y, or FP32
-//    split-K partials for the library's second pass.
-// Every wait is bounded on the global timer.  A wait that runs out sets bit 2
-// of the error word; the CTA stops issuing, waits (bounded) for the copies it
-// issued, writes NaN to its outputs and frees its tensor memory before it
-// returns.  The accumulation order depends on (K range, stage width) only.
+//  * W never passes through registers.  A producer thread streams boxes of
+//    128 rows x 64 elements of W (16 KiB) with cp.async.bulk.tensor into a
+//    ring of S shared-memory stages of NB boxes each, 128-byte swizzled, with
+//    the matching 16 x 64 box of x (2 KiB; rows >= M and columns >= K are
+//    zero-filled by the copy engine, so they cost no memory traffic).  Each
+//    stage completes on its "full" mbarrier.
+//  * One thread issues, per box, four tcgen05.mma.kind::f16 of 128 (rows of
+//    W) x 16 (rows of x, padded) x 16 (k), both operands K-major in shared
+//    memory, FP32 accumulator in tensor memory, then tcgen05.commit onto the
+//    stage's "empty" mbarrier, which hands the stage back to the producer.
+//    At a tile's end it commits onto the tile's accumulator barrier.
+//  * Four epilogue warps read the 128 x 16 accumulator with tcgen05.ld (warp
+//    w reads tensor-memory lanes 32(w%4) .. +31, the tile's rows) and write y
+//    through the library's common epilogue (BF16, FP32, or the fused decode-
+//    chain step).  Two accumulators alternate, so the epilogue of one tile
+//    overlaps the MMAs of the next.
+//  * Work split, one of two forms (both one launch, no scratch memory):
+//     - split == 1: a persistent grid; each CTA takes a balanced contiguous
+//       range of 128-row tiles and walks each tile's whole K;
+//     - split > 1: the `split` CTAs of a thread-block cluster share one tile,
+//       each a contiguous range of K boxes.  At the end every CTA but rank 0
+//       stores its FP32 partial tile into rank 0's shared memory
+//       (distributed shared memory), a cluster barrier orders the stores, and
+//       rank 0 adds the partials in rank order and writes y.
+//
+// The accumulation order of an output depends on (K, boxes per split) only:
+// never on M (the columns of one MMA are independent), the ring depth, the
+// boxes per stage or the grid.  So results are deterministic and row m of an
+// M-row call equals the 1-row call.
+//
+// Every wait on an mbarrier is bounded on the global timer.  A wait that runs
+// out sets bit 0 of the device error word; the CTA stops issuing, writes NaN
+// to its outputs, waits (bounded) for the copies and MMAs it issued and frees
+// its tensor memory before it returns, so the context stays usable.  The
+// test-only flag kFlagTestStall makes the producer issue no copies, so the
+// waits run out without any fault.
 #pragma once
 
 #include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
 #include "skinny_ldg.cuh"
+#include "tc05_consts.h"
 
 namespace sk {
 namespace tc05 {
 
-constexpr int kRows = 128;                        // rows of W per tile (MMA M)
-constexpr int kCols = 16;                         // columns of the MMA (rows of x, padded)
-constexpr int kBoxK = 64;                         // K elements per stage (128 bytes of a row)
-constexpr int kWBytes = kRows * kBoxK * 2;        // 16 KiB
-constexpr int kXBytes = kCols * kBoxK * 2;        // 2 KiB
-constexpr int kStageBytes = kWBytes + kXBytes;    // multiple of 1024 (swizzle atoms)
-constexpr int kTmemCols = 32;                     // smallest allocation
-constexpr int kThreads = 128;                     // four warps
-
-struct Tc05Params {
-    CUtensorMap tw;   // W [N][K]: dims {K, N}, box {64, 128}, 128-byte swizzle
-    CUtensorMap tx;   // x [M][K]: dims {K, M}, box {64, 16}, 128-byte swizzle
-    uint16_t *y;      // [M][ldy] BF16, written when split == 1
-    long long ldy;
-    float *ws;        // [split][M][N] FP32 partials when split > 1
-    int M, N, K;
-    int kps;          // K elements per split, a multiple of 64
-    int split;
-    int stages;       // ring depth S
-    int flags;
-    int *err;
-};
-
-// Shared-memory matrix descriptor of a K-major operand laid out in 128-byte
-// swizzle atoms (8 rows x 128 bytes, 1024 bytes apart along the rows):
-// start address >> 4 (bits 0-13), leading byte offset (unused by this layout,
-// 1), stride byte offset 1024 >> 4 (bits 32-45), descriptor version 1 (bits
-// 46-47), layout 128-byte swizzle = 2 (bits 61-63).
+// Shared-memory matrix descriptor of a K-major operand stored in 128-byte
+// swizzle atoms (8 rows x 128 bytes; atoms 1024 bytes apart along the rows):
+// start address >> 4 (bits 0-13), leading byte offset 1 (unused by this
+// layout, bits 16-29), stride byte offset 1024 >> 4 (bits 32-45), descriptor
+// version 1 (bits 46-47), base offset 0, layout 128-byte swizzle = 2 (bits
+// 61-63).  Advancing K by 16 elements inside the atom adds 32 bytes to the
+// start address; the swizzle is applied to the generated addresses.
+constexpr uint64_t kDescHi = (static_cast<uint64_t>(1024 >> 4) << 32) |
+                             (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(1) << 16;
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
-    return d;
+    return kDescHi | (static_cast<uint64_t>(1) << 16) |
+           static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
 }
 
 // Instruction descriptor of tcgen05.mma.kind::f16: FP32 accumulator (bits 4-5
@@ -93,6 +84,10 @@ __device__ __forceinline__ uint32_t saddr(const void *p) {
 
 __device__ __forceinline__ void bar_init(uint32_t b, unsigned count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void bar_arrive(uint32_t b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(b) : "memory");
 }
 
 __device__ __forceinline__ void bar_expect_tx(uint32_t b, unsigned bytes) {
@@ -112,7 +107,8 @@ __device__ __forceinline__ bool bar_try(uint32_t b, unsigned parity) {
     return ok != 0;
 }
 
-// Wait for phase `parity` of mbarrier b, at most kWaitLimitNs.
+// Wait for the phase of parity `parity` of mbarrier b to complete, at most
+// kWaitLimitNs; false when the wait ran out.
 __device__ __forceinline__ bool bar_wait(uint32_t b, unsigned parity) {
     if (bar_try(b, parity)) return true;
     const unsigned long long t0 = global_ns();
@@ -120,6 +116,10 @@ __device__ __forceinline__ bool bar_wait(uint32_t b, unsigned parity) {
         if (static_cast<long long>(global_ns() - t0) > kWaitLimitNs) return false;
     }
     return true;
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -132,246 +132,322 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t tmem, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t idesc, uint32_t accumulate) {
+                                        uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
         : "memory");
 }
 
+// Arrive on mbarrier b once every tcgen05 operation this thread issued so far
+// has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::
                      "r"(bar)
                  : "memory");
 }
 
-template <int M>
-__global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_constant__ Tc05Params p) {
-    static_assert(M >= 1 && M <= kCols, "x rows fill the N columns of the MMA");
-    extern __shared__ uint8_t smem_raw[];
-    // the swizzled stages want 1024-byte alignment of their shared-memory
-    // addresses; the host adds 1 KiB of slack
-    uint8_t *smem = smem_raw + ((1024u - (saddr(smem_raw) & 1023u)) & 1023u);
-    const int S = p.stages;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * kStageBytes);  // full[S], empty[S], done
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * S + 1);
-    __shared__ int abort_flag;
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const bool pdl = (p.flags & kFlagPdl) != 0;
-    if (pdl) pdl_launch_dependents();
-
-    const int n0 = blockIdx.x * kRows;
-    const int k0 = blockIdx.y * p.kps;
-    const int kc = min(p.K - k0, p.kps);
-    const int nst = (kc + kBoxK - 1) / kBoxK;  // stages of this CTA
-
-    if (threadIdx.x == 0) {
-        abort_flag = 0;
-        for (int s = 0; s < 2 * S + 1; ++s) bar_init(saddr(bars + s), 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         saddr(tmem_slot)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+__device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
+}
+__device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const uint32_t tmem = *tmem_slot;
+}
 
-    if (pdl) pdl_wait();  // x (and y) belong to the stream's previous kernel
-
-    int issued = 0;  // stages the producer issued
-    if (warp == 0 && lane == 0) {
-        // producer: stage st goes to slot st % S; refilling a slot waits for the
-        // MMAs that read it (phase (st / S - 1) & 1 of its "empty" barrier)
-        for (int st = 0; st < nst; ++st) {
-            const int slot = st % S;
-            if (st >= S && !bar_wait(saddr(bars + S + slot), ((st / S) - 1) & 1)) {
-                atomicExch(&abort_flag, 1);
-                break;
-            }
-            if (atomicAdd(&abort_flag, 0)) break;
-            uint8_t *stage = smem + slot * kStageBytes;
-            const uint32_t full = saddr(bars + slot);
-            bar_expect_tx(full, kStageBytes);
-            tma_load_2d(saddr(stage), &p.tw, k0 + st * kBoxK, n0, full);
-            tma_load_2d(saddr(stage + kWBytes), &p.tx, k0 + st * kBoxK, 0, full);
-            ++issued;
-        }
-    } else if (warp == 1 && lane == 0) {
-        // MMA issuer: four K = 16 steps per stage, 32 bytes apart in the swizzled rows
-        bool ok = true;
-        for (int st = 0; st < nst; ++st) {
-            const int slot = st % S;
-            if (!bar_wait(saddr(bars + slot), (st / S) & 1)) {
-                ok = false;
-                break;
-            }
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            uint8_t *stage = smem + slot * kStageBytes;
-            const uint32_t a0 = saddr(stage), b0 = saddr(stage + kWBytes);
-#pragma unroll
-            for (int j = 0; j < kBoxK / 16; ++j)
-                mma_f16(tmem, sw128_desc(a0 + 32 * j), sw128_desc(b0 + 32 * j), kIdesc,
-                        (st > 0 || j > 0) ? 1u : 0u);
-            mma_commit(saddr(bars + S + slot));
-        }
-        if (!ok) atomicExch(&abort_flag, 1);
-        mma_commit(saddr(bars + 2 * S));  // "done" once every issued MMA has completed
-    }
-
-    // epilogue: every warp waits for "done", then reads its 32 rows x 16 columns.
-    // tcgen05.ld is warp-wide: the warp reconverges first (lane 0 of warps 0 and 1
-    // comes from its own loop, and each lane leaves the bounded wait on its own).
-    bool done_ok = bar_wait(saddr(bars + 2 * S), 0);
-    __syncwarp();
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    uint32_t r[16];
+// 16 consecutive FP32 columns of this thread's tensor-memory lane (warp-wide).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
           "=r"(r[14]), "=r"(r[15])
-        : "r"(tmem + (static_cast<uint32_t>(warp * 32) << 16)));
+        : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
 
-    const bool bad = !done_ok || atomicAdd(&abort_flag, 0) != 0;
-    if (bad && threadIdx.x == 0 && p.err) atomicOr(p.err, 4);
-    const int n = n0 + warp * 32 + lane;  // this thread's row of the tile
-    if (n < p.N) {
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+// Store v at CTA-local shared address `local` of the cluster's CTA `rank`.
+__device__ __forceinline__ void st_cluster_f32(uint32_t local, uint32_t rank, float v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ int read_flag(const int *f) {
+    return *reinterpret_cast<const volatile int *>(f);
+}
+
+template <int M>
+__global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_constant__ Tc05Params p) {
+    static_assert(M >= 1 && M <= 8, "x rows fill the first M columns of the MMA");
+    extern __shared__ uint8_t smem_raw[];
+    // full[S], empty[S], accumulator full[2], accumulator empty[2], MMAs done
+    __shared__ __align__(8) uint64_t bars[2 * kMaxRingSlots + 5];
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    // swizzled stages want 1024-byte aligned shared addresses; the host adds 1 KiB of slack
+    uint8_t *ring = smem_raw + ((1024u - (saddr(smem_raw) & 1023u)) & 1023u);
+    const int S = p.ring;
+    const int NB = p.nb;
+    const int stage_bytes = NB * kBoxBytes;
+    float *red = reinterpret_cast<float *>(ring + S * stage_bytes);  // [split-1][M][128]
+
+    const Params &bp = p.base;
+    const int bi = blockIdx.y;  // problem of a batched call
+    const Item &it = bp.item[bi];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const bool pdl = (bp.flags & kFlagPdl) != 0;
+    if (pdl) pdl_launch_dependents();
+
+    // this CTA's tiles and K boxes
+    const int split = p.split;
+    int t_begin, t_end, kb0, kb1;
+    uint32_t rank = 0;
+    if (split > 1) {
+        rank = cluster_rank();
+        t_begin = static_cast<int>(blockIdx.x) / split;
+        t_end = t_begin + 1;
+        kb0 = static_cast<int>(rank) * p.per;
+        kb1 = min(p.kbox, kb0 + p.per);
+    } else {
+        t_begin = static_cast<int>(static_cast<long long>(p.tiles) * blockIdx.x / gridDim.x);
+        t_end = static_cast<int>(static_cast<long long>(p.tiles) * (blockIdx.x + 1) / gridDim.x);
+        kb0 = 0;
+        kb1 = p.kbox;
+    }
+    const int nbox = kb1 - kb0;
+    const int nst = (nbox + NB - 1) / NB;  // stages per tile
+    const int ntile = t_end - t_begin;
+    const int total = ntile * nst;         // stages of this CTA
+
+    const uint32_t full0 = saddr(&bars[0]);
+    const uint32_t empty0 = full0 + 8 * S;
+    const uint32_t accf0 = full0 + 8 * 2 * kMaxRingSlots;
+    const uint32_t acce0 = accf0 + 16;
+    const uint32_t fin = acce0 + 16;
+
+    // The producer is thread 0.  Its tensor maps, and the stage -> (rows, boxes) map.
+    const CUtensorMap *tw = &p.tw[bi];
+    const CUtensorMap *tx = &p.tx[bi];
+    const bool stall = (bp.flags & kFlagTestStall) != 0;
+    auto stage_of = [&](int g, int &row, int &kb, int &cnt) {
+        const int t = g / nst;
+        const int st = g - t * nst;
+        row = (t_begin + t) * kRows;
+        kb = kb0 + st * NB;
+        cnt = min(NB, kb1 - kb);
+    };
+    auto issue_w = [&](int g) {
+        int row, kb, cnt;
+        stage_of(g, row, kb, cnt);
+        const int slot = g % S;
+        const uint32_t fb = full0 + 8 * slot;
+        bar_expect_tx(fb, static_cast<unsigned>(cnt * kBoxBytes));
+        if (stall) return;
+        const uint32_t st0 = saddr(ring + slot * stage_bytes);
+        for (int b = 0; b < cnt; ++b) tma_load_2d(st0 + b * kWBox, tw, (kb + b) * kBoxK, row, fb);
+    };
+    auto issue_x = [&](int g) {
+        if (stall) return;
+        int row, kb, cnt;
+        stage_of(g, row, kb, cnt);
+        const int slot = g % S;
+        const uint32_t x0 = saddr(ring + slot * stage_bytes) + NB * kWBox;
+        for (int b = 0; b < cnt; ++b)
+            tma_load_2d(x0 + b * kXBox, tx, (kb + b) * kBoxK, 0, full0 + 8 * slot);
+    };
+    // W of the first ring's worth of stages may stream before the previous kernel
+    // on the stream finishes (PDL with read-only weights); x may not
+    const bool early_w = !pdl || (bp.flags & kFlagWeightsReadOnly);
+    const int pre = early_w ? min(S, total) : 0;
+
+    if (threadIdx.x == 0) {
+        prefetch_tmap(tw);
+        prefetch_tmap(tx);
+        abort_flag = 0;
+        for (int s = 0; s < S; ++s) {
+            bar_init(full0 + 8 * s, 1);
+            bar_init(empty0 + 8 * s, 1);
+        }
+        bar_init(accf0, 1);
+        bar_init(accf0 + 8, 1);
+        bar_init(acce0, 4);
+        bar_init(acce0 + 8, 4);
+        bar_init(fin, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the copy engine
+        // the first loads go out before the tensor-memory allocation and the CTA barrier
+        for (int g = 0; g < pre; ++g) issue_w(g);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         saddr(&tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    if (split > 1) cluster_arrive_relaxed();  // this CTA has started (paired with the wait below)
+
+    float v[M];  // split > 1: this thread's partial sums of its row, kept for the cluster reduce
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-            const float v = bad ? __int_as_float(0x7fc00000) : __uint_as_float(r[m]);
-            if (p.split == 1) {
-                p.y[m * p.ldy + n] = f32_to_bf16_rn(v);
-            } else {
-                p.ws[(static_cast<long long>(blockIdx.y) * M + m) * p.N + n] = v;
+    for (int m = 0; m < M; ++m) v[m] = 0.0f;
+
+    int issued = 0;  // stages the producer issued
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0 && total > 0) {
+            if (pdl) pdl_wait();
+            for (int g = 0; g < pre; ++g) issue_x(g);
+            issued = pre;
+            for (int g = pre; g < total; ++g) {
+                const int slot = g % S;
+                if (g >= S && !bar_wait(empty0 + 8 * slot, ((g / S) - 1) & 1)) {
+                    atomicExch(&abort_flag, 1);
+                    break;
+                }
+                if (read_flag(&abort_flag)) break;
+                issue_w(g);
+                issue_x(g);
+                issued = g + 1;
+            }
+            if (stall) issued = 0;  // nothing is in flight
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            bool ok = true;
+            int g = 0;
+            for (int i = 0; i < ntile && ok; ++i) {
+                const int b = i & 1;
+                if (i >= 2 && !bar_wait(acce0 + 8 * b, ((i >> 1) - 1) & 1)) {
+                    atomicExch(&abort_flag, 1);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(b * kCols);
+                for (int st = 0; st < nst; ++st, ++g) {
+                    const int slot = g % S;
+                    if (!bar_wait(full0 + 8 * slot, (g / S) & 1) || read_flag(&abort_flag)) {
+                        atomicExch(&abort_flag, 1);  // before the commit below releases the epilogue
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int cnt = min(NB, nbox - st * NB);
+                    const uint32_t a0 = saddr(ring + slot * stage_bytes);
+                    const uint32_t x0 = a0 + NB * kWBox;
+                    for (int bx = 0; bx < cnt; ++bx) {
+#pragma unroll
+                        for (int j = 0; j < kBoxK / 16; ++j)
+                            mma_f16(d, sw128_desc(a0 + bx * kWBox + 32 * j),
+                                    sw128_desc(x0 + bx * kXBox + 32 * j),
+                                    (st | bx | j) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(empty0 + 8 * slot);
+                }
+                // also on failure, so that the epilogue's wait for this tile ends
+                mma_commit(accf0 + 8 * b);
+            }
+            // every MMA issued has completed before the tensor memory is freed
+            mma_commit(fin);
+            if (!bar_wait(fin, 0)) atomicExch(&abort_flag, 1);
+        }
+    } else {
+        // --------------------------------------------------------------- epilogue
+        if (pdl) pdl_wait();  // y (and the fused next input) may be read by the previous kernel
+        const int q = warp & 3;  // tensor-memory lane quarter this warp may access
+        const int row = q * 32 + lane;
+        for (int i = 0; i < ntile; ++i) {
+            const int b = i & 1;
+            bool good = !read_flag(&abort_flag) && bar_wait(accf0 + 8 * b, (i >> 1) & 1) &&
+                        !read_flag(&abort_flag);
+            good = __all_sync(0xffffffffu, good);  // tcgen05.ld is warp-wide
+            uint32_t r[16];
+            if (good) {
+                tc_fence_after();
+                tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * kCols), r);
+                tc_fence_before();
+            }
+            __syncwarp();
+            if (lane == 0) bar_arrive(acce0 + 8 * b);
+            if (!good && lane == 0) atomicExch(&abort_flag, 1);
+#pragma unroll
+            for (int m = 0; m < M; ++m) v[m] = good ? __uint_as_float(r[m]) : __int_as_float(0x7fc00000);
+            if (split == 1) {
+                const int n = (t_begin + i) * kRows + row;
+                if (n < bp.N) {
+#pragma unroll
+                    for (int m = 0; m < M; ++m) store_out(bp, it, m, n, v[m]);
+                }
+            }
+        }
+    }
+    __syncwarp();
+
+    if (split > 1) {
+        // deterministic K reduction across the cluster: ranks 1.. store their partial
+        // tile into rank 0's shared memory, rank 0 adds them in rank order
+        cluster_wait_acquire();  // every CTA of the cluster has started
+        if (warp >= 2 && rank > 0 && ntile > 0) {
+            const int row = (warp & 3) * 32 + lane;
+#pragma unroll
+            for (int m = 0; m < M; ++m)
+                st_cluster_f32(saddr(red + ((rank - 1) * M + m) * kRows + row), 0u, v[m]);
+        }
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        if (warp >= 2 && rank == 0 && ntile > 0) {
+            const int row = (warp & 3) * 32 + lane;
+            const int n = t_begin * kRows + row;
+            if (n < bp.N) {
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    float s = v[m];
+                    for (int rr = 1; rr < split; ++rr) s += red[((rr - 1) * M + m) * kRows + row];
+                    store_out(bp, it, m, n, s);
+                }
             }
         }
     }
 
-    // on the abort path: the producer's copies must have landed before the CTA's
-    // shared memory goes, and the issued MMAs must be done before their tensor
-    // memory is freed (both bounded)
-    if (warp == 0 && lane == 0 && bad) {
-        for (int st = max(0, issued - S); st < issued; ++st)
-            (void)bar_wait(saddr(bars + st % S), (st / S) & 1);
+    // abort path: the producer's copies must have landed before the CTA's shared
+    // memory goes (bounded waits); the MMAs are known complete (the "done" barrier)
+    if (warp == 0 && lane == 0 && read_flag(&abort_flag)) {
+        for (int g = max(0, issued - S); g < issued; ++g)
+            (void)bar_wait(full0 + 8 * (g % S), (g / S) & 1);
     }
-    if (warp == 1 && lane == 0 && !done_ok) (void)bar_wait(saddr(bars + 2 * S), 0);
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0 && abort_flag && bp.err) atomicOr(bp.err, 1);
     if (warp == 1) {
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols)
                      : "memory");
     }
-}
-
-// Dynamic shared memory of a CTA with S stages: the ring, 2S+1 mbarriers, the
-// tensor-memory address slot, and 1 KiB of alignment slack.
-inline size_t smem_bytes(int stages) {
-    return static_cast<size_t>(stages) * kStageBytes + (2 * stages + 1) * 8 + 16 + 1024;
-}
-
-// Host: the two tensor maps of one problem.  The driver's encoder is looked up
-// through the runtime once, so the library needs no link against the driver
-// library.  W [N][K] row-major: dims {K, N}, row stride 2K bytes, box {64, 128};
-// x [M][K] with row stride ldx: dims {K, M}, box {64, 16}.  Both 128-byte
-// swizzled (a box row is exactly 128 bytes), out-of-range elements read as 0.
-// The preconditions of the library's calls (16-byte aligned x and W, K and ldx
-// multiples of 8) are those of the encoder.
-inline cudaError_t encode_maps(Tc05Params &p, const uint16_t *x, long long ldx, const uint16_t *W,
-                               int M, int N, int K) {
-    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-    if (!encode) {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                         cudaEnableDefault, &q);
-        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
-        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-    const cuuint32_t estride[2] = {1, 1};
-    {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-        const cuuint32_t box[2] = {kBoxK, kRows};
-        if (encode(&p.tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(W), dims,
-                   strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx) * 2};
-        const cuuint32_t box[2] = {kBoxK, kCols};
-        if (encode(&p.tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims,
-                   strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    return cudaSuccess;
-}
-
-// Host: one launch of the kernel for y = x . W^T (one problem), M <= 16.
-// grid = (ceil(N / 128) tiles, split); split > 1 writes FP32 partials to ws
-// ([split][M][N], caller-provided) for the library's split-K second pass,
-// which the caller launches after this.  kps (K per split) is rounded up to
-// whole 64-element stages, so the splits actually used (stored in *split_used
-// when given; the second pass must use that count) may be fewer than asked.
-// Flags as Params::flags (PDL launch attribute when kFlagPdl is set).  Returns
-// the launch's CUDA status.
-template <int M>
-inline cudaError_t launch(const uint16_t *x, long long ldx, const uint16_t *W, uint16_t *y,
-                          long long ldy, int N, int K, int split, int stages, float *ws,
-                          int *err, int flags, cudaStream_t stream, int *split_used = nullptr) {
-    Tc05Params p;
-    cudaError_t e = encode_maps(p, x, ldx, W, M, N, K);
-    if (e != cudaSuccess) return e;
-    const int nst = (K + kBoxK - 1) / kBoxK;
-    const int per = (nst + split - 1) / split;
-    p.y = y;
-    p.ldy = ldy;
-    p.ws = ws;
-    p.M = M;
-    p.N = N;
-    p.K = K;
-    p.kps = per * kBoxK;
-    p.split = (nst + per - 1) / per;  // every split non-empty
-    if (split_used) *split_used = p.split;
-    p.stages = stages;
-    p.flags = flags;
-    p.err = err;
-    const size_t smem = smem_bytes(stages);
-    e = cudaFuncSetAttribute(skinny_tc05_kernel<M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((N + kRows - 1) / kRows),
-                       static_cast<unsigned>(p.split), 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    if (flags & kFlagPdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    return cudaLaunchKernelEx(&cfg, skinny_tc05_kernel<M>, p);
 }
 
 }  // namespace tc05

@@ -50,6 +50,11 @@ BULK_GEOMETRY = [(16, 8), (32, 4), (32, 6), (64, 2), (64, 3)]
 # warp-owned-tile tensor-core kernel: warps sharing a tile's K range x CTAs per SM
 TW_SPLITS = [1, 2, 4, 8]
 TW_CTAS = [0, 1, 2]
+# TMA + tcgen05 kernel: (ring slots, 64-element boxes per stage), cluster splits of K,
+# and CTAs per SM of the persistent grid (split 1 only)
+TC05_GEOMETRY = [(4, 1), (6, 1), (8, 1), (12, 1), (3, 2), (4, 2), (6, 2), (2, 4), (3, 4)]
+TC05_SPLITS = [1, 2, 3, 4, 6, 8, 16]
+TC05_CTAS = [0, 1, 2]
 
 
 def candidates(M, N, K, splits):
@@ -60,6 +65,12 @@ def candidates(M, N, K, splits):
             variants = [base.copy(k_unroll=kb, stages=ring) for kb, ring in BULK_GEOMETRY]
         elif base.variant == sk.SGEMM_VARIANT_MMA_TW:
             variants = [base.copy(split_k=s, ctas_per_sm=c) for s in TW_SPLITS for c in TW_CTAS]
+        elif base.variant == sk.SGEMM_VARIANT_TC05:
+            if base.k_unroll != 1:
+                continue  # the enumeration lists this kernel twice; its geometry is swept here
+            variants = [base.copy(stages=r, k_unroll=nb, split_k=s, ctas_per_sm=c)
+                        for r, nb in TC05_GEOMETRY for s in TC05_SPLITS
+                        for c in (TC05_CTAS if s == 1 else [0])]
         else:
             variants = [base.copy(split_k=s) for s in splits]
         for p in variants:

@@ -112,7 +112,7 @@ enum {
                                      the x-as-A MMA on it.  threads = 32 * (1 + consumer warps),
                                      rows_per_warp = 8, lanes_per_row = 4, k_unroll = stage width
                                      in 32-element k-blocks, stages = ring slots (2..16),
-                                     split_k = 1.  Needs the library scratch for its error word */
+                                     split_k = 1 */
     SGEMM_VARIANT_LDG_FFMA2 = 5,  /* the streaming kernel of variant 0 with packed FP32x2 FMA
                                      (two partial sums per output, even and odd k, added at the
                                      end): half the FMA instructions */
@@ -129,13 +129,29 @@ enum {
                                      k-blocks of a row); they add their fragments in shared
                                      memory, in order, with no second pass and no scratch.
                                      rows_per_warp = 8, lanes_per_row = 4 */
-    SGEMM_VARIANT_LDG_MMA = 9     /* the streaming kernel of variant 1 (one row's 512 bytes per
+    SGEMM_VARIANT_LDG_MMA = 9,    /* the streaming kernel of variant 1 (one row's 512 bytes per
                                      load instruction, lanes_per_row = 32) with the products
                                      done by mma.sync m16n8k16: the 8 columns of B are the 8
                                      consecutive 32-element segments a warp load covers, A holds
                                      x rows m and m+1 at the same k, and the diagonal of D is the
                                      per-segment dot product (2 MMAs per 16 bytes of W and pair
                                      of x rows, instead of 8 FMAs per x row) */
+    SGEMM_VARIANT_TC05 = 10       /* the Blackwell tensor-core data path: a producer thread streams
+                                     boxes of 128 rows x 64 elements of W (and the matching box
+                                     of x) with TMA (cp.async.bulk.tensor) into a ring of shared-
+                                     memory stages; one thread issues tcgen05.mma (128 rows of W x
+                                     16 columns of x, FP32 accumulator in tensor memory); four
+                                     warps read the accumulator back and write y.  No W element
+                                     passes through registers.  threads = 192, rows_per_warp =
+                                     128 (rows per tile), lanes_per_row = 0, k_unroll = boxes
+                                     per stage (1, 2 or 4), stages = ring slots (2..16).
+                                     split_k = 1: a persistent grid of ctas_per_sm CTAs per SM
+                                     (0 = occupancy) over the tiles; split_k = 2..16: the split_k
+                                     CTAs of a thread-block cluster share a tile's K range (in
+                                     whole 64-element boxes; ceil(ceil(K/64) / ceil(ceil(K/64) /
+                                     split_k)) ranges are used) and add their partial sums in
+                                     rank order through distributed shared memory: one launch,
+                                     no scratch memory */
 };
 
 /* Launch flags (bit set) for the _ex calls.
@@ -152,9 +168,11 @@ enum {
  *   kernel finishes. */
 #define SGEMM_FLAG_PDL 1u
 #define SGEMM_FLAG_WEIGHTS_READONLY 2u
-/* TEST ONLY: bulk-copy kernels (SGEMM_VARIANT_BULK) issue no copies, so their
- * bounded waits run out (about 0.2 s); they then write NaN outputs, set the
- * device error word and return.  Exercises failure detection without a fault. */
+/* TEST ONLY: the kernels that wait on mbarriers for copies (SGEMM_VARIANT_BULK
+ * and SGEMM_VARIANT_TC05) issue no copies, so their bounded waits run out
+ * (about 0.2 s each); they then write NaN outputs, set the device error word
+ * and return.  Exercises failure detection without a fault.  Other variants
+ * ignore the flag. */
 #define SGEMM_FLAG_TEST_STALL 4u
 
 /* y = x . W^T for contiguous x [M,K] and y [M,N].  Plan: sgemm_plan_select(N, K, M). */
@@ -303,9 +321,11 @@ sgemm_status_t sgemm_bf16_skinny_splitk_noalloc(const sgemm_bf16_t *x, long long
                                                 sgemm_stream_t stream);
 
 /* Reads and clears the device error word of the current device: bit 0 is set
- * when a bulk-copy kernel gave up waiting for its data (its outputs were
- * written as NaN).  *flags = 0 when nothing went wrong or no such kernel ran.
- * Synchronous (waits for the device); do not call during stream capture. */
+ * when a kernel gave up a bounded wait for its data (SGEMM_VARIANT_BULK or
+ * SGEMM_VARIANT_TC05; the outputs of that launch were written as NaN).
+ * *flags = 0 when nothing went wrong.  The word is a static device variable
+ * of the library (no allocation).  Synchronous (waits for the device); do not
+ * call during stream capture. */
 sgemm_status_t sgemm_device_errors(int *flags);
 
 /* Static description of a status code (never NULL). */

@@ -8,7 +8,6 @@ from __future__ import annotations
 import ctypes
 import os
 import re
-import subprocess
 
 import pytest
 
@@ -203,24 +202,39 @@ def test_heuristic_plan_splits_k_when_rows_leave_sms_idle(lib):
         assert sk.sgemm_plan_check(p, M, 3000, 2000) == sk.SGEMM_OK
 
 
-def test_tensor_core_draft_compiles_for_sm103a(tmp_path):
-    """The TMA + tcgen05 kernel draft (csrc/skinny_tc05.cuh), not yet part of
-    the library, compiles for sm_103a: ptxas accepts its tensor-memory,
-    bulk-tensor and mbarrier instruction forms."""
-    src = tmp_path / "tc05.cu"
-    src.write_text('#include "skinny_tc05.cuh"\n'
-                   'const void *tc05_kernels[] = {\n'
-                   '    (const void *)&sk::tc05::skinny_tc05_kernel<1>,\n'
-                   '    (const void *)&sk::tc05::skinny_tc05_kernel<4>,\n'
-                   '    (const void *)&sk::tc05::skinny_tc05_kernel<8>};\n'
-                   'cudaError_t tc05_launch_m4(const uint16_t *x, const uint16_t *W, uint16_t *y,\n'
-                   '                           int N, int K, cudaStream_t s) {\n'
-                   '    return sk::tc05::launch<4>(x, K, W, y, N, N, K, 1, 4, nullptr, nullptr, 0, s);\n'
-                   '}\n')
-    cmd = [skbuild.nvcc(), *skbuild.ARCH_FLAGS, "-O3", "-std=c++17", "-I", skbuild.CSRC,
-           "-I", skbuild.INCLUDE, "-c", str(src), "-o", str(tmp_path / "tc05.o")]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    assert r.returncode == 0, r.stdout + r.stderr
+def _tc05_plan():
+    for i in range(sk.sgemm_plan_count()):
+        p = sk.sgemm_plan_get(i)
+        if p.variant == sk.SGEMM_VARIANT_TC05:
+            return p
+    raise AssertionError("no TC05 plan enumerated")
+
+
+def test_tc05_plan_checks(lib):
+    """Host-side checks of the TMA + tcgen05 plans: fixed geometry (192
+    threads, 128-row tiles), 1/2/4 boxes per stage, 2..16 ring slots that fit
+    shared memory, and a cluster split of 1..16 with at least one 64-element
+    box of K per split."""
+    p = _tc05_plan()
+    assert (p.threads, p.rows_per_warp, p.lanes_per_row) == (192, 128, 0)
+    for M in range(1, 9):
+        assert sk.sgemm_plan_check(p, M, 4096, 4096) == sk.SGEMM_OK
+    for split in (1, 2, 3, 5, 8, 16):
+        assert sk.sgemm_plan_check(p.copy(split_k=split), 4, 613, 2600) == sk.SGEMM_OK
+    for change in ({"threads": 256}, {"rows_per_warp": 64}, {"lanes_per_row": 32},
+                   {"k_unroll": 3}, {"k_unroll": 8}, {"stages": 1}, {"stages": 17},
+                   {"split_k": 0}, {"split_k": 17}, {"ctas_per_sm": -1}, {"vec_bytes": 8},
+                   {"stages": 16, "k_unroll": 4}):
+        bad = p.copy(**change)
+        assert sk.sgemm_plan_check(bad, 1, 4096, 4096) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE, change
+        assert _call_plan(lib, bad) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE, change
+    # K = 64 is one box: no split; K = 72 is two boxes
+    assert sk.sgemm_plan_check(p.copy(split_k=2), 1, 16, 64) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE
+    assert sk.sgemm_plan_check(p.copy(split_k=2), 1, 16, 72) == sk.SGEMM_OK
+    # the largest ring that fits: 12 single-box stages (12 x 18 KiB + slack)
+    assert sk.sgemm_plan_check(p.copy(stages=12, k_unroll=1), 8, 4096, 4096) == sk.SGEMM_OK
+    assert sk.sgemm_plan_check(p.copy(stages=6, k_unroll=2, split_k=16), 8, 4096, 4096) == \
+        sk.SGEMM_ERR_UNSUPPORTED_SHAPE  # plus 15 x 8 x 128 floats of cluster partials
 
 
 def test_plan_table_round_trip(tmp_path):

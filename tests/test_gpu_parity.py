@@ -350,7 +350,8 @@ def test_plans_with_same_lanes_per_row_agree_bitwise(M):
             y = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=plan)
             torch.cuda.synchronize()
             mma = plan.variant in (sk.SGEMM_VARIANT_MMA, sk.SGEMM_VARIANT_MMA_T,
-                                   sk.SGEMM_VARIANT_BULK, sk.SGEMM_VARIANT_MMA_TW)
+                                   sk.SGEMM_VARIANT_BULK, sk.SGEMM_VARIANT_MMA_TW,
+                                   sk.SGEMM_VARIANT_TC05)
             # the widened and the mixed-precision FMA round identically; the packed
             # FP32x2 FMA keeps two partial sums, a different order of its own
             ffma2 = plan.variant in (sk.SGEMM_VARIANT_LDG_FFMA2, sk.SGEMM_VARIANT_LDGX_FFMA2)
