@@ -2,17 +2,21 @@
 
 Default workload (one "step"): the decode-shape sweep at M = 1, 2, 4 over the
 local (N, K) shapes (12576,4096), (4096,4096), (2048,4096), (4096,1024),
-(8192,1536), (4096,8192).  Following the measurement protocol of vLLM PR
+(8192,1536), (4096,8192), plus the LM head (77440,4096) at M = 1, 2, 4.
+Following the measurement protocol of vLLM PR
 #65306 (Validation: each case is a chain over copies of the weight adding up to
 at least 1 GiB, captured in a CUDA graph) and PR #62949 (Validation: cold-L2
 numbers, the weight rotated out of L2), every (shape, M) is a CUDA graph of R
 GEMMs, each on its own weight copy, with R copies totalling
 >= max(1 GiB, 4 x L2).  So every GEMM reads its weights from HBM.
 
-Reported (one JSON line on rank 0):
+Reported on rank 0: a compact table (per shape: us per GEMM, fraction of the
+HBM peak and time relative to M=1, at each M; then the paired projection and
+the decode chain, timed after the step) followed by one JSON line:
 - value: algorithmic bytes (W + x + y) of the whole step / device time, GB/s,
   summed over ranks (replicas: each GPU runs the whole sweep);
-- detail: per (N, K, M) cold-L2 us per GEMM, GB/s and fraction of HBM peak;
+- detail (only in the --detail-out file): per (N, K, M) cold-L2 us per GEMM,
+  GB/s, fraction of HBM peak, the plan, and the pairs and chain results;
 - roofline: the skinny kernel's achieved GB/s against the measured HBM peak;
 - e2e: the same metric with every step's x copied in from pinned host memory
   and every y copied back, through the library's public call;
@@ -54,6 +58,14 @@ FALLBACK_HBM_GBS = 6800.0
 def gemm_bytes(M, N, K):
     """Algorithmic bytes of one GEMM: W + x + y, BF16."""
     return 2 * (N * K + M * K + M * N)
+
+
+def launches_per_gemm(sk, plan):
+    """Kernel launches of one GEMM: split-K plans of the streaming and 16-row
+    tensor-core kernels add a second-pass reduce; the tcgen05 kernel reduces
+    its K split inside a cluster and the warp-owned-tile kernel inside a CTA."""
+    one_launch = (sk.SGEMM_VARIANT_TC05, sk.SGEMM_VARIANT_MMA_TW)
+    return 2 if plan.split_k > 1 and plan.variant not in one_launch else 1
 
 
 # --------------------------------------------------------------------- helpers
@@ -114,7 +126,8 @@ def measured_peaks():
 # The streaming kernels' sources, their compiled configurations, the plan table and
 # the launch geometry: what the recorded DRAM traffic per launch depends on.
 KERNEL_SOURCES = ["skinny_ldg.cuh", "skinny_mma.cuh", "skinny_mmat.cuh", "skinny_mmatw.cuh",
-                  "skinny_bulk.cuh", "kernel_table.cuh", "internal.h", "plan_table.inc", "api.cpp"]
+                  "skinny_tc05.cuh", "tc05_consts.h", "tc05_launch.cu",
+                  "kernel_table.cuh", "internal.h", "plan_table.inc", "api.cpp"]
 
 
 def kernel_source_hash():
@@ -237,7 +250,7 @@ class GraphSet:
         self.x_host.copy_(self.x_pack.cpu())
 
     def launches_per_step(self):
-        return sum(c["R"] * (2 if c["plan"].split_k > 1 else 1) for c in self.cases)
+        return sum(c["R"] * launches_per_gemm(self.sk, c["plan"]) for c in self.cases)
 
     def capture(self, flags_list):
         """One graph per (case, launch flags); the GEMMs go through the public
@@ -362,10 +375,11 @@ def reference_arm(args):
     ws, rank, _ = dist_info()
     if rank != 0:
         return 0
-    cases = [(N, K, M) for (N, K) in SWEEP_SHAPES for M in SWEEP_MS]
+    shapes = list(SWEEP_SHAPES) + ([] if args.no_lmhead else [LMHEAD])
+    cases = [(N, K, M) for (N, K) in shapes for M in SWEEP_MS]
     rows = args.reference_rows
     W = {(N, K): synth.bits(synth.normal_bf16((min(rows, N), K), synth.W_STD, seed=0))
-         for (N, K) in SWEEP_SHAPES}
+         for (N, K) in shapes}
     X = {(K, M): synth.bits(synth.normal_bf16((M, K), 1.0, seed=M)) for (_, K, M) in cases}
     threads = oracle.cores()
 
@@ -390,11 +404,12 @@ def reference_arm(args):
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(t / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": sweep_config_desc(None),
+            "config": dict(sweep_config_desc(None, lmhead=not args.no_lmhead),
+                           launch_flags=args.flags),
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": used,
                              "kind": "oracle",
-                             "sample": f"each step: the first {rows} W rows of each of the 18 "
-                                       f"(N,K,M) sweep GEMMs, all M rows of x"},
+                             "sample": f"each step: the first {rows} W rows of each of the "
+                                       f"{len(cases)} (N,K,M) GEMMs of the step, all M rows of x"},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -440,7 +455,7 @@ def _capture(torch, fn):
     return g
 
 
-def run_pairs(args, torch, sk, synth, dist, min_bytes):
+def pairs_result(args, torch, sk, synth, dist, min_bytes):
     """Paired projection f_b / g_b, (N, K) = (4096, 128), M = 1..4: both problems
     in ONE batched launch, against two separate launches of the same kernel
     (vLLM PR #57617, Microbenchmark table: two Linear calls vs one paired call).
@@ -499,16 +514,10 @@ def run_pairs(args, torch, sk, synth, dist, min_bytes):
                        "launch_flags": "pdl,readonly", "parallelism": "replicas"},
             "gpu_launches": sum(d["copies"] * 3 for d in detail) * args.steps,
             "detail": detail}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-        if args.detail_out:
-            with open(args.detail_out, "w") as f:
-                json.dump(line, f, indent=1)
-    dist.close()
-    return 0
+    return line
 
 
-def run_chain(args, torch, sk, synth, dist):
+def chain_result(args, torch, sk, synth, dist):
     """Decode-step chain at M=1: 186 GEMMs on distinct weights in the order
     (12576,4096)x34, (4096,4096)x34, (2048,4096)x53, (4096,1024)x42,
     (8192,1536)x11, (4096,8192)x11, (77440,4096)x1 (7.5 GB of weights, so every
@@ -585,7 +594,12 @@ def run_chain(args, torch, sk, synth, dist):
                                     "epilogue (sgemm_bf16_skinny_rescale_ex), whole step, "
                                     "nothing subtracted; outputs bitwise equal"},
             "gpu_launches": ((2 * len(seq) - 1) + (len(seq) - 1) + len(seq)) * args.steps}
-    if rank == 0:
+    return line
+
+
+def emit(line, args, dist):
+    """Print the JSON line on rank 0 (and write it to --detail-out), then close."""
+    if dist_info()[1] == 0:
         print(json.dumps(line), flush=True)
         if args.detail_out:
             with open(args.detail_out, "w") as f:
@@ -594,19 +608,42 @@ def run_chain(args, torch, sk, synth, dist):
     return 0
 
 
-def sweep_config_desc(gs):
+def run_pairs(args, torch, sk, synth, dist, min_bytes):
+    return emit(pairs_result(args, torch, sk, synth, dist, min_bytes), args, dist)
+
+
+def run_chain(args, torch, sk, synth, dist):
+    return emit(chain_result(args, torch, sk, synth, dist), args, dist)
+
+
+def sweep_config_desc(gs, lmhead=True):
     d = {"workload": "shape sweep at M=1,2,4 over local (N,K) = " +
-                     ", ".join(f"({N},{K})" for N, K in SWEEP_SHAPES),
+                     ", ".join(f"({N},{K})" for N, K in SWEEP_SHAPES) +
+                     (" and the LM head (77440,4096)" if lmhead else ""),
          "x": "BF16 ~ N(0,1)", "W": "BF16 ~ N(0,0.02^2)", "seed": 0,
-         "l2": "inputs larger than L2: each GEMM reads its own weight copy; copies per shape "
-               "total >= max(1 GiB, 4 x L2)",
-         "timing": "CUDA graph per (N,K,M) of R GEMMs on R copies; CUDA events per graph",
-         "launch": "sgemm_bf16_skinny_ex with the selected plan; the timed chains use the launch "
-                   "flags in 'launch_flags' (weights are never written inside the chain)",
+         "l2": "inputs larger than L2: each GEMM reads its own weight copy, copies per shape "
+               ">= max(1 GiB, 4 x L2)",
+         "timing": "a CUDA graph of R GEMMs per (N,K,M); CUDA events",
          "parallelism": "replicas"}
-    if gs is not None:
-        d["copies"] = {f"{c['N']}x{c['K']}": c["R"] for c in gs.cases if c["M"] == 1}
     return d
+
+
+def compact_table(detail, peak, extras):
+    """Short per-shape lines for stdout: us per GEMM, fraction of the HBM peak
+    and time relative to M=1, at each M."""
+    lines = [f"# cold-L2 us per GEMM / fraction of {peak:.0f} GB/s / time vs M=1 (plan variant)"]
+    shapes = []
+    for d in detail:
+        if (d["N"], d["K"]) not in shapes:
+            shapes.append((d["N"], d["K"]))
+    for (N, K) in shapes:
+        row = [d for d in detail if d["N"] == N and d["K"] == K]
+        cells = " ".join(f"M{d['M']} {d['us']:.2f}/{d['frac']:.3f}/{d.get('time_vs_m1', 1.0):.2f}"
+                         f"(v{d['plan']['variant']})" for d in row)
+        lines.append(f"# {N}x{K} {cells}")
+    for e in extras:
+        lines.append("# " + e)
+    return lines
 
 
 def run_router(args, torch, sk, synth, dist, min_bytes):
@@ -715,7 +752,7 @@ def run_wide(args, torch, sk, synth, dist, min_bytes):
                            "plan": {"variant": p.variant, "threads": p.threads,
                                     "k_unroll": p.k_unroll, "split_k": p.split_k, "id": p.id}})
             nbytes += R * gemm_bytes(M, N, K)
-            launches += R * (2 if p.split_k > 1 and p.variant != sk.SGEMM_VARIANT_MMA_TW else 1)
+            launches += R * launches_per_gemm(sk, p)
     per, _ = _time_graphs(torch, dist, graphs, args.steps, args.warmup)
     del graphs, keep
     peak, _ = measured_peaks()
@@ -770,6 +807,10 @@ def main():
     ap.add_argument("--no-plain", action="store_true",
                     help="skip the extra timing of plain launches (no launch flags)")
     ap.add_argument("--detail-out", default=None, help="also write the full result JSON here")
+    ap.add_argument("--no-lmhead", action="store_true",
+                    help="leave the LM head (77440,4096) out of the default step")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the paired-projection and decode-chain lines after the step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -795,7 +836,9 @@ def main():
     min_bytes = max(args.min_bytes, 4 * l2)
 
     if args.workload == "sweep":
-        shapes = SWEEP_SHAPES
+        shapes = list(SWEEP_SHAPES)
+        if not args.no_lmhead:
+            shapes.append(LMHEAD)
         if args.shapes:
             shapes = [tuple(int(v) for v in t.split("x")) for t in args.shapes.split(",")]
         ms = [int(v) for v in args.ms.split(",")] if args.ms else SWEEP_MS
@@ -847,9 +890,7 @@ def main():
         detail.append({"N": c["N"], "K": c["K"], "M": c["M"], "copies": c["R"],
                        "us": round(us, 3), "gbs": round(b / us / 1e3, 1),
                        "frac": round(b / us / 1e3 / peak, 4), **extra,
-                       "plan": {k: v for k, v in c["plan"].as_dict().items()
-                                if k in ("threads", "rows_per_warp", "lanes_per_row", "k_unroll",
-                                         "split_k", "id")}})
+                       "plan": c["plan"].as_dict()})
         kern_bytes += c["R"] * b * len(ms)
         kern_ms += sum(ms)
         key = (c["N"], c["K"], c["M"])
@@ -884,20 +925,43 @@ def main():
         cpu, _ = cpu_baseline(gs.cases)
         cpu["value"] = round(cpu["value"], 4)
 
+    # the paired projection and the decode chain, timed after the step (not in value)
+    extras, extra_detail = [], {}
+    if args.workload == "sweep" and not args.no_extras:
+        pr = pairs_result(args, torch, sk, synth, dist, min_bytes)
+        extra_detail["pairs"] = pr
+        extras.append("pairs 2x(4096,128) us/launch " + " ".join(
+            f"M{d['M']} {d['us_per_paired_launch']:.2f}" for d in pr["detail"]) +
+            " (two launches: " + " ".join(f"{d['us_two_launches']:.2f}" for d in pr["detail"]) + ")")
+        ch = chain_result(args, torch, sk, synth, dist)
+        extra_detail["chain"] = ch
+        c = ch["chain"]
+        extras.append(f"chain 186 GEMMs M=1: fused step {c['fused_step_us']:.0f} us "
+                      f"({c['fused_frac_of_peak']:.3f} of peak), separate {c['step_us']:.0f} us, "
+                      f"GEMMs alone {c['gemm_us']:.0f} us ({c['frac_of_peak']:.3f})")
+
+    config = (sweep_config_desc(gs, lmhead=LMHEAD in [(c["N"], c["K"]) for c in gs.cases])
+              if args.workload == "sweep" else
+              {"workload": f"{args.workload}: " + ", ".join(f"M={m} ({n},{k})" for n, k, m in cases),
+               "l2": "inputs larger than L2 (rotating weight copies)", "parallelism": "replicas"})
+    config["launch_flags"] = args.flags
+    roofline.pop("traffic_note", None)
+    if cpu is not None:
+        cpu["sample"] = cpu["sample"].split(";")[0]
     line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(total_s / args.steps * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": dict(sweep_config_desc(gs), launch_flags=args.flags) if args.workload == "sweep" else
-            {"workload": f"{args.workload}: " + ", ".join(f"M={m} ({n},{k})" for n, k, m in cases),
-             "l2": "inputs larger than L2 (rotating weight copies)", "parallelism": "replicas"},
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": n_launch,
-            "clocks": clocks, "detail": detail}
+            "config": config, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": n_launch, "clocks": clocks}
     if rank == 0:
+        for ln in compact_table(detail, peak, extras):
+            print(ln, flush=True)
         print(json.dumps(line), flush=True)
         if args.detail_out:
             with open(args.detail_out, "w") as f:
-                json.dump(line, f, indent=1)
+                json.dump(dict(line, detail=detail, traffic_source=traffic_src, **extra_detail),
+                          f, indent=1)
     dist.close()
     return 0
 

@@ -23,11 +23,12 @@ __all__ = [
     "sgemm_bf16_skinny", "sgemm_bf16_skinny_ex", "sgemm_bf16_skinny_batched",
     "sgemm_bf16_skinny_batched_ex", "sgemm_plan_select", "sgemm_plan_count", "sgemm_plan_get",
     "sgemm_plan_check", "sgemm_init", "sgemm_status_string", "sgemm_version",
-    "sgemm_bf16_skinny_splitk_noalloc", "NOALLOC_SCRATCH_BYTES", "sgemm_bf16_rescale",
+    "sgemm_bf16_skinny_splitk_noalloc", "sgemm_splitk_noalloc_plan", "NOALLOC_SCRATCH_BYTES",
+    "sgemm_bf16_rescale",
     "sgemm_bf16_skinny_rescale_ex", "sgemm_bf16_skinny_f32out_ex",
     "SGEMM_OK", "SGEMM_ERR_INVALID_ARG", "SGEMM_ERR_UNSUPPORTED_SHAPE", "SGEMM_ERR_MISALIGNED",
     "SGEMM_ERR_UNSUPPORTED_DEVICE", "SGEMM_ERR_NO_WORKSPACE", "SGEMM_ERR_CUDA", "MAX_BATCH",
-    "SGEMM_VARIANT_LDG", "SGEMM_VARIANT_LDG_MIXFMA", "SGEMM_VARIANT_MMA", "SGEMM_VARIANT_MMA_T", "SGEMM_VARIANT_BULK", "SGEMM_VARIANT_LDG_FFMA2", "SGEMM_VARIANT_LDGX_MIXFMA",
+    "SGEMM_VARIANT_LDG", "SGEMM_VARIANT_LDG_MIXFMA", "SGEMM_VARIANT_MMA", "SGEMM_VARIANT_MMA_T", "SGEMM_VARIANT_LDG_FFMA2", "SGEMM_VARIANT_LDGX_MIXFMA",
     "SGEMM_VARIANT_LDGX_FFMA2", "SGEMM_VARIANT_MMA_TW", "SGEMM_VARIANT_LDG_MMA",
     "SGEMM_VARIANT_TC05", "SGEMM_FLAG_PDL",
     "SGEMM_FLAG_TEST_STALL", "sgemm_device_errors",
@@ -46,7 +47,6 @@ SGEMM_VARIANT_LDG = 0
 SGEMM_VARIANT_LDG_MIXFMA = 1
 SGEMM_VARIANT_MMA = 2
 SGEMM_VARIANT_MMA_T = 3
-SGEMM_VARIANT_BULK = 4
 SGEMM_VARIANT_LDG_FFMA2 = 5
 SGEMM_VARIANT_LDGX_MIXFMA = 6
 SGEMM_VARIANT_LDGX_FFMA2 = 7
@@ -142,6 +142,9 @@ def load() -> ctypes.CDLL:
         lib.sgemm_status_string.restype = ctypes.c_char_p
         lib.sgemm_bf16_skinny_splitk_noalloc.argtypes = [vp, ll, vp, vp, ll, ci, ci, ci, ci, vp]
         lib.sgemm_bf16_skinny_splitk_noalloc.restype = ci
+        lib.sgemm_splitk_noalloc_plan.argtypes = [ci, ci, ci, ci, ctypes.POINTER(Plan),
+                                                  ctypes.POINTER(Plan)]
+        lib.sgemm_splitk_noalloc_plan.restype = ci
         lib.sgemm_bf16_rescale.argtypes = [vp, ll, vp, ll, ctypes.c_float, cu, vp]
         lib.sgemm_bf16_rescale.restype = ci
         lib.sgemm_device_errors.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -328,7 +331,7 @@ def sgemm_bf16_skinny_splitk_noalloc(x: torch.Tensor, W: torch.Tensor,
     on a device (which looks the array up) should come before stream capture.
     ``y`` must be given for the call itself to allocate nothing (otherwise this
     wrapper creates it with torch).  Results equal ``sgemm_bf16_skinny_ex`` with
-    the same split.
+    the plan :func:`sgemm_splitk_noalloc_plan` returns.
     """
     M, N, K, y = _problem(x, W, y)
     need = int(split_k) * M * N * 4
@@ -342,6 +345,18 @@ def sgemm_bf16_skinny_splitk_noalloc(x: torch.Tensor, W: torch.Tensor,
                                                    ldy, M, N, K, int(split_k), _stream(stream)),
            "sgemm_bf16_skinny_splitk_noalloc")
     return y
+
+
+def sgemm_splitk_noalloc_plan(N: int, K: int, M: int, split_k: int,
+                              selected: Plan | None = None) -> tuple[int, Plan]:
+    """(status, plan): the plan :func:`sgemm_bf16_skinny_splitk_noalloc` runs for
+    this problem, from ``selected`` (default: the selected plan) with split_k
+    splits through scratch memory (host-only)."""
+    out = Plan()
+    st = load().sgemm_splitk_noalloc_plan(int(N), int(K), int(M), int(split_k),
+                                          ctypes.byref(selected) if selected is not None else None,
+                                          ctypes.byref(out))
+    return st, out
 
 
 def sgemm_plan_select(N: int, K: int, M: int) -> Plan:

@@ -58,7 +58,7 @@ const KernelInfo *table_for_m(int M) {
 const KernelInfo *find_kernel(int variant, int M, int R, int LPR, int U, int stages) {
     const KernelInfo *t = table_for_m(M);
     if (!t) return nullptr;
-    if (variant == SGEMM_VARIANT_BULK || variant == SGEMM_VARIANT_TC05) {
+    if (variant == SGEMM_VARIANT_TC05) {
         // one kernel per M; the rest are launch parameters
         for (int i = 0; i < sk::kKernelCountPerM; ++i)
             if (t[i].variant == variant && t[i].R == R && t[i].LPR == LPR) return &t[i];
@@ -87,20 +87,6 @@ std::mutex g_mu;
 std::map<int, DeviceState> g_dev;
 
 
-sgemm_status_t check_bulk_plan(const sgemm_plan_t &p, int M, int K) {
-    const int nw = p.threads / 32 - 1;
-    if (p.threads % 32 || nw < 2 || p.threads > sk::kMaxThreadsBulk) return SGEMM_ERR_UNSUPPORTED_SHAPE;
-    if (p.rows_per_warp != 8 || p.lanes_per_row != 4 || p.vec_bytes != 16)
-        return SGEMM_ERR_UNSUPPORTED_SHAPE;
-    if (p.k_unroll < 1 || p.k_unroll > 128 || p.stages < 2 || p.stages > sk::kMaxRing)
-        return SGEMM_ERR_UNSUPPORTED_SHAPE;
-    if (p.split_k != 1 || p.ctas_per_sm < 0 || p.ctas_per_sm > 2) return SGEMM_ERR_UNSUPPORTED_SHAPE;
-    if (!find_kernel(p.variant, M, 8, 4, 0, 0)) return SGEMM_ERR_UNSUPPORTED_SHAPE;
-    // leave 1 KiB for the kernel's static shared memory
-    if (sk::smem_bytes(p, M, K) + 1024 > kMaxSmem) return SGEMM_ERR_UNSUPPORTED_SHAPE;
-    return SGEMM_OK;
-}
-
 sgemm_status_t check_tc05_plan(const sgemm_plan_t &p, int M, int K) {
     if (p.threads != sk::tc05::kThreads || p.rows_per_warp != sk::tc05::kRows ||
         p.lanes_per_row != 0 || p.vec_bytes != 16)
@@ -121,7 +107,6 @@ sgemm_status_t check_tc05_plan(const sgemm_plan_t &p, int M, int K) {
 
 sgemm_status_t check_plan(const sgemm_plan_t &p, int M, int N, int K) {
     (void)N;
-    if (p.variant == SGEMM_VARIANT_BULK) return check_bulk_plan(p, M, K);
     if (p.variant == SGEMM_VARIANT_TC05) return check_tc05_plan(p, M, K);
     if (p.variant != SGEMM_VARIANT_LDG && p.variant != SGEMM_VARIANT_LDG_MIXFMA &&
         p.variant != SGEMM_VARIANT_LDG_FFMA2 && p.variant != SGEMM_VARIANT_MMA &&
@@ -405,11 +390,10 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
                                        plan.k_unroll, plan.stages);
     if (plan.variant == SGEMM_VARIANT_TC05) return run_tc05(items, batch, M, N, K, plan, flags,
                                                             stream, ep, *st, ki->fn);
-    const bool bulk = plan.variant == SGEMM_VARIANT_BULK;
     const bool tw = plan.variant == SGEMM_VARIANT_MMA_TW;  // split_k splits K inside a CTA
     const int split = tw ? 1 : plan.split_k;
-    const int kps = bulk ? 32 * plan.k_unroll : (tw ? K : sk::split_kps(K, split));
-    const size_t smem = sk::smem_bytes(plan, M, bulk ? K : kps);
+    const int kps = tw ? K : sk::split_kps(K, split);
+    const size_t smem = sk::smem_bytes(plan, M, kps);
 
     sk::Params prm;
     std::memset(&prm, 0, sizeof(prm));
@@ -431,7 +415,6 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
     prm.split = tw ? plan.split_k : split;
     prm.row_groups = sk::work_units(plan, N);
     prm.flags = static_cast<int>(flags);
-    prm.ring = bulk ? plan.stages : 0;
 
     int grid_x = 0;
     {
@@ -447,13 +430,11 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
             if (sk::allow_max_dynamic_smem(ki->fn) != cudaSuccess) return SGEMM_ERR_CUDA;
             st->smem_attr_set[ki->fn] = true;
         }
-        const int occ = (plan.ctas_per_sm > 0 && !bulk)
-                            ? plan.ctas_per_sm
-                            : occupancy(*st, ki->fn, plan.threads, smem);
+        const int occ = plan.ctas_per_sm > 0 ? plan.ctas_per_sm
+                                             : occupancy(*st, ki->fn, plan.threads, smem);
         const long long need_ctas = sk::ctas_wanted(plan, N);
-        const int occ_eff = bulk ? std::min(occ, std::max(plan.ctas_per_sm, 1)) : occ;
         const long long slots = std::max<long long>(
-            1, static_cast<long long>(st->sms) * occ_eff / (static_cast<long long>(split) * batch));
+            1, static_cast<long long>(st->sms) * occ / (static_cast<long long>(split) * batch));
         grid_x = static_cast<int>(std::max<long long>(1, std::min(need_ctas, slots)));
     }
 
@@ -506,11 +487,6 @@ int split_kps(int K, int split) {
 }
 
 size_t smem_bytes(const sgemm_plan_t &plan, int M, int kps) {
-    if (plan.variant == SGEMM_VARIANT_BULK) {
-        // kps is the whole K here: the bulk kernel keeps all of x in shared memory
-        const BulkLayout L(M, kps, 32 * plan.k_unroll, plan.stages, plan.threads / 32 - 1);
-        return static_cast<size_t>(L.total);
-    }
     const size_t chunks = static_cast<size_t>(kps) / 8;
     if (plan.variant == SGEMM_VARIANT_LDGX_MIXFMA || plan.variant == SGEMM_VARIANT_LDGX_FFMA2)
         return 0;  // x is read from global memory
@@ -535,8 +511,7 @@ size_t smem_bytes(const sgemm_plan_t &plan, int M, int kps) {
 int work_units(const sgemm_plan_t &plan, int N) {
     if (plan.variant == SGEMM_VARIANT_TC05) return (N + tc05::kRows - 1) / tc05::kRows;
     if (plan.variant == SGEMM_VARIANT_MMA) return (N + 15) / 16;
-    if (plan.variant == SGEMM_VARIANT_MMA_T || plan.variant == SGEMM_VARIANT_BULK ||
-        plan.variant == SGEMM_VARIANT_MMA_TW)
+    if (plan.variant == SGEMM_VARIANT_MMA_T || plan.variant == SGEMM_VARIANT_MMA_TW)
         return (N + 7) / 8;
     const int rows_per_task = (32 / plan.lanes_per_row) * plan.rows_per_warp;
     return (N + rows_per_task - 1) / rows_per_task;
@@ -553,7 +528,7 @@ cudaError_t allow_max_dynamic_smem(const void *fn) {
 long long ctas_wanted(const sgemm_plan_t &plan, int N) {
     const long long units = work_units(plan, N);
     if (plan.variant == SGEMM_VARIANT_MMA || plan.variant == SGEMM_VARIANT_MMA_T ||
-        plan.variant == SGEMM_VARIANT_BULK || plan.variant == SGEMM_VARIANT_TC05)
+        plan.variant == SGEMM_VARIANT_TC05)
         return units;  // one tile per CTA at most
     if (plan.variant == SGEMM_VARIANT_MMA_TW) {
         const int groups = std::max(1, plan.threads / 32 / std::max(1, plan.split_k));
@@ -584,12 +559,6 @@ int sgemm_plan_count(void) { return sk::kKernelCountPerM * kNumThreadChoices; }
 sgemm_status_t sgemm_plan_get(int index, sgemm_plan_t *plan) {
     if (!plan || index < 0 || index >= sgemm_plan_count()) return SGEMM_ERR_INVALID_ARG;
     const KernelInfo &k = sk::kKernelsM1[index / kNumThreadChoices];
-    if (k.variant == SGEMM_VARIANT_BULK) {
-        // producer warp + 8 or 4 consumer warps; 1024-wide stages, 4 ring slots
-        const int threads = (index % kNumThreadChoices) == 0 ? 288 : 160;
-        *plan = make_plan(k.variant, threads, 8, 4, 32, 1, 4, 0, -1);
-        return SGEMM_OK;
-    }
     if (k.variant == SGEMM_VARIANT_TC05) {
         // six single-box stages, or three stages of two boxes (the same bytes in flight)
         const bool first = (index % kNumThreadChoices) == 0;

@@ -14,8 +14,6 @@ namespace sk {
 constexpr int kMaxBatch = SGEMM_MAX_BATCH;
 constexpr int kMaxM = 8;
 constexpr int kMaxThreads = 256;
-constexpr int kMaxThreadsBulk = 288;  // producer warp + up to 8 consumer warps
-constexpr int kMaxRing = 16;          // ring slots of the bulk-copy kernel
 constexpr size_t kMaxSmemOptin = 227 * 1024;  // shared memory a CTA may opt in to
 
 // One problem of a (possibly batched) launch.  Row strides in elements.
@@ -44,8 +42,7 @@ struct Params {
     int split;       // number of K splits (gridDim.y)
     int row_groups;  // ceil(N / rows per warp task)
     int flags;       // SGEMM_FLAG_* bits
-    int ring;        // bulk-copy kernel: shared-memory ring slots
-    int *err;        // bulk-copy kernel: device error word (bit 0: a wait gave up); may be null
+    int *err;        // device error word (bit 0: a bounded wait gave up); may be null
     int out_f32;     // 1: y holds FP32 outputs (no BF16 rounding)
     int xn_len;      // fused chain epilogue: xn[m][k] for 0 <= k < xn_len ...
     float xn_scale;  // ... = RNE_bf16(float(y[m][k mod N]) * xn_scale)
@@ -64,31 +61,6 @@ struct alignas(64) Tc05Params {
     int split;                  // CTAs per cluster sharing a tile (1 = persistent grid)
     int ring;                   // shared-memory stages
     int nb;                     // boxes per stage
-};
-
-#ifdef __CUDACC__
-#define SK_HD __host__ __device__
-#else
-#define SK_HD
-#endif
-
-// Shared-memory layout of one CTA (all offsets 16-byte aligned):
-//   [0, 256)          mbarriers: full[S], empty[S]  (S <= 16)
-//   x                 M rows of K BF16, row stride K*2 + 16 bytes
-//   ring              S slots of 8 rows x KS BF16, row stride KS*2 + 16 bytes
-//   partials          2 x NW x 8 x M floats
-struct BulkLayout {
-    int S, KS, NW;
-    long long x_off, x_stride, ring_off, row_stride, slot_bytes, red_off, total;
-    SK_HD BulkLayout(int M, int K, int KS_, int S_, int NW_) : S(S_), KS(KS_), NW(NW_) {
-        x_off = 256;
-        x_stride = 2LL * K + 16;
-        ring_off = x_off + M * x_stride;
-        row_stride = 2LL * KS + 16;
-        slot_bytes = 8 * row_stride;
-        red_off = ring_off + S * slot_bytes;
-        total = red_off + 2LL * NW * 8 * M * 4;
-    }
 };
 
 // A compiled instantiation of a kernel template.

@@ -10,7 +10,6 @@
 #include "skinny_ldg.cuh"
 #include "skinny_mma.cuh"
 #include "skinny_mmat.cuh"
-#include "skinny_bulk.cuh"
 #include "skinny_mmatw.cuh"
 #include "skinny_tc05.cuh"
 
@@ -109,11 +108,6 @@
     {SGEMM_VARIANT_MMA_T, M, 8, 4, U, (DB) ? 2 : 1,        \
      reinterpret_cast<const void *>(&skinny_mmat_kernel<M, U, DB>)},
 
-// Bulk-copy pipelined kernel: one instantiation per M; ring depth, stage
-// width and consumer warps are launch parameters (U = 0, stages = 0 mark "any").
-#define SK_BULK_ENTRY(M) \
-    {SGEMM_VARIANT_BULK, M, 8, 4, 0, 0, reinterpret_cast<const void *>(&skinny_bulk_kernel<M>)},
-
 // TMA + tcgen05 kernel: one instantiation per M; tile rows 128, and the ring
 // depth, boxes per stage and cluster split are launch parameters (U = 0,
 // stages = 0 mark "any").
@@ -122,7 +116,7 @@
 
 #define SK_DEFINE_TABLE(M, NAME)                                                          \
     const KernelInfo NAME[] = {SK_LDG_CONFIGS(SK_LDG_ENTRY, M) SK_MMA_CONFIGS(SK_MMA_ENTRY, M) \
-                                   SK_MMAT_CONFIGS(SK_MMAT_ENTRY, M) SK_BULK_ENTRY(M)     \
+                                   SK_MMAT_CONFIGS(SK_MMAT_ENTRY, M)     \
                                        SK_LDGX_CONFIGS(SK_LDGX_ENTRY, M)   \
                                            SK_MMATW_CONFIGS(SK_MMATW_ENTRY, M) \
                                                SK_TC05_ENTRY(M)};

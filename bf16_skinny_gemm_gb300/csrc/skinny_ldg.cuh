@@ -369,7 +369,11 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
 
     Batch bufA, bufB;
     const bool early_w = !pdl || (p.flags & kFlagWeightsReadOnly);
+    // with read-only weights, both batches of a double-buffered plan go out before
+    // the wait for the previous kernel (the same order the loop below would use)
+    const bool pre_b = DB && early_w && U < total;
     if (early_w) issue_batch(bufA, 0);
+    if (pre_b) issue_batch(bufB, U);
     if (pdl) pdl_wait();
     if (!early_w) issue_batch(bufA, 0);
 
@@ -470,7 +474,7 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
         // consumed (the two buffers are distinct registers, so consuming one does not
         // wait for the other's loads)
         for (int base = 0; base < total; base += 2 * U) {
-            if (base + U < total) issue_batch(bufB, base + U);
+            if (base + U < total && !(base == 0 && pre_b)) issue_batch(bufB, base + U);
             consume_batch(bufA, base);
             if (base + U >= total) break;
             if (base + 2 * U < total) issue_batch(bufA, base + 2 * U);

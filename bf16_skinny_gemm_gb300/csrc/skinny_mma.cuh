@@ -98,7 +98,11 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mma_kernel(const __grid_co
 
     Batch bA, bB;
     const bool early_w = !pdl || (p.flags & kFlagWeightsReadOnly);
+    // with read-only weights, both batches of a double-buffered plan go out before
+    // the wait for the previous kernel (the same order the loop below would use)
+    const bool pre_b = DB && early_w && U < total;
     if (early_w) issue_batch(bA, 0);
+    if (pre_b) issue_batch(bB, U);
     if (pdl) pdl_wait();
     if (!early_w) issue_batch(bA, 0);
 
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mma_kernel(const __grid_co
         // the next batch is in flight while this one is consumed, including the
         // tile-end barrier and reduction
         for (int base = 0; base < total; base += 2 * U) {
-            if (base + U < total) issue_batch(bB, base + U);
+            if (base + U < total && !(base == 0 && pre_b)) issue_batch(bB, base + U);
             consume_batch(bA, base);
             if (base + U >= total) break;
             if (base + 2 * U < total) issue_batch(bA, base + 2 * U);

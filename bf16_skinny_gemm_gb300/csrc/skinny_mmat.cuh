@@ -88,7 +88,11 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mmat_kernel(const __grid_c
 
     Batch wA, wB;
     const bool early_w = !pdl || (p.flags & kFlagWeightsReadOnly);
+    // with read-only weights, both batches of a double-buffered plan go out before
+    // the wait for the previous kernel (the same order the loop below would use)
+    const bool pre_b = DB && early_w && U < total;
     if (early_w) issue_batch(wA, 0);
+    if (pre_b) issue_batch(wB, U);
     if (pdl) pdl_wait();
     if (!early_w) issue_batch(wA, 0);
 
@@ -151,7 +155,7 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_mmat_kernel(const __grid_c
 
     if (DB) {
         for (int base = 0; base < total; base += 2 * U) {
-            if (base + U < total) issue_batch(wB, base + U);
+            if (base + U < total && !(base == 0 && pre_b)) issue_batch(wB, base + U);
             consume_batch(wA, base);
             if (base + U >= total) break;
             if (base + 2 * U < total) issue_batch(wA, base + 2 * U);

@@ -11,16 +11,16 @@
 // instead uses the file-scope array below, which is part of the library's
 // device image and is created when the library's code is loaded on a device.
 //
-// The kernels are the regular ones of the selected plan (the streaming kernel
-// with gridDim.y splits, then splitk_reduce_kernel; a CUDA-core plan when the
-// selected one is the bulk-copy kernel, which cannot split K, and the x-as-A
-// tensor-core kernel with CTA-wide tiles when the selected one is its
-// warp-owned-tile form, whose split_k splits K inside a CTA); only where the
-// FP32 partial sums live differs, so results are bitwise equal to
+// The kernels are the regular ones of the plan sgemm_splitk_noalloc_plan
+// returns: the selected plan with split_k splits (the kernel with gridDim.y
+// splits, then splitk_reduce_kernel), or a plan that splits K the same way
+// when the selected one does not (see that function); only where the FP32
+// partial sums live differs, so results are bitwise equal to
 // sgemm_bf16_skinny_ex with that plan.
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <set>
 
 #include "internal.h"
 
@@ -40,6 +40,7 @@ struct DeviceSetup {
     bool supported = false;
     int sms = 0;
     float *scratch = nullptr;  // device address of g_splitk_scratch on this device
+    std::set<const void *> smem_attr_set;  // kernels already allowed their shared memory
 };
 
 std::mutex g_mu;
@@ -68,14 +69,19 @@ const sk::KernelInfo *find(int M, const sgemm_plan_t &p) {
 
 // Once per device, with that device current: look up the array's device
 // address (the host-side name g_splitk_scratch is only a stand-in and must
-// never be handed to a kernel) and allow the kernels their shared memory.
-sgemm_status_t setup_current_device(DeviceSetup **out) {
+// never be handed to a kernel).  Refused while `stream` is capturing, so that
+// the one-time set-up never lands inside a graph.  Then allow the kernel `fn`
+// its shared memory (once per kernel and device).
+sgemm_status_t setup_current_device(cudaStream_t stream, const void *fn, DeviceSetup **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_UNSUPPORTED_DEVICE;
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceSetup &st = g_dev[dev];
     if (!st.done) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return SGEMM_ERR_CUDA;
+        if (cap != cudaStreamCaptureStatusNone) return SGEMM_ERR_INVALID_ARG;
         int major = 0, minor = 0, sms = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -88,21 +94,55 @@ sgemm_status_t setup_current_device(DeviceSetup **out) {
             if (cudaGetSymbolAddress(&ptr, g_splitk_scratch) != cudaSuccess || ptr == nullptr)
                 return SGEMM_ERR_CUDA;
             st.scratch = static_cast<float *>(ptr);
-            const sk::KernelInfo *tables[] = {sk::kKernelsM1, sk::kKernelsM2, sk::kKernelsM3,
-                                              sk::kKernelsM4, sk::kKernelsM5, sk::kKernelsM6,
-                                              sk::kKernelsM7, sk::kKernelsM8};
-            for (const sk::KernelInfo *t : tables)
-                for (int i = 0; i < sk::kKernelCountPerM; ++i)
-                    if (sk::allow_max_dynamic_smem(t[i].fn) != cudaSuccess) return SGEMM_ERR_CUDA;
         }
         st.done = true;
     }
     if (!st.supported) return SGEMM_ERR_UNSUPPORTED_DEVICE;
+    if (!st.smem_attr_set.count(fn)) {
+        if (sk::allow_max_dynamic_smem(fn) != cudaSuccess) return SGEMM_ERR_CUDA;
+        st.smem_attr_set.insert(fn);
+    }
     *out = &st;
     return SGEMM_OK;
 }
 
+sgemm_plan_t streaming_plan(int split_k) {
+    sgemm_plan_t p;
+    p.variant = SGEMM_VARIANT_LDG_MIXFMA;
+    p.threads = 256;
+    p.rows_per_warp = 1;
+    p.lanes_per_row = 32;
+    p.k_unroll = 8;
+    p.vec_bytes = 16;
+    p.split_k = split_k;
+    p.stages = 1;
+    p.ctas_per_sm = 0;
+    p.id = -1;
+    return p;
+}
+
 }  // namespace
+
+extern "C" sgemm_status_t sgemm_splitk_noalloc_plan(int N, int K, int M, int split_k,
+                                                    const sgemm_plan_t *selected,
+                                                    sgemm_plan_t *out) {
+    if (!out || split_k < 2) return SGEMM_ERR_INVALID_ARG;
+    sgemm_plan_t plan = selected ? *selected : sgemm_plan_select(N, K, M);
+    plan.split_k = split_k;
+    if (plan.variant == SGEMM_VARIANT_TC05) {
+        // the tcgen05 kernel reduces its split inside a cluster, without scratch: the
+        // CUDA-core streaming kernel with split_k splits
+        plan = streaming_plan(split_k);
+    } else if (plan.variant == SGEMM_VARIANT_MMA_TW) {
+        // its split_k splits K inside a CTA: the x-as-A kernel with CTA-wide tiles and
+        // the same math, at most 8 k-blocks per batch (the unrolls that kernel has)
+        plan.variant = SGEMM_VARIANT_MMA_T;
+        if (plan.k_unroll > 8) plan.k_unroll = 8;
+        plan.ctas_per_sm = 0;
+    }
+    *out = plan;
+    return sgemm_plan_check(out, M, N, K);
+}
 
 extern "C" sgemm_status_t sgemm_bf16_skinny_splitk_noalloc(
     const sgemm_bf16_t *x, long long ldx, const sgemm_bf16_t *W, sgemm_bf16_t *y, long long ldy,
@@ -118,29 +158,15 @@ extern "C" sgemm_status_t sgemm_bf16_skinny_splitk_noalloc(
     if (static_cast<unsigned long long>(split_k) * M * N > kScratchFloats)
         return SGEMM_ERR_UNSUPPORTED_SHAPE;
 
-    sgemm_plan_t plan = sgemm_plan_select(N, K, M);
-    plan.split_k = split_k;
-    if (plan.variant == SGEMM_VARIANT_BULK) {
-        // the bulk-copy kernel does not split K: use the CUDA-core streaming kernel
-        plan.variant = SGEMM_VARIANT_LDG_MIXFMA;
-        plan.threads = 256;
-        plan.rows_per_warp = 1;
-        plan.lanes_per_row = 32;
-        plan.k_unroll = 8;
-        plan.stages = 1;
-        plan.ctas_per_sm = 0;
-    }
-    if (plan.variant == SGEMM_VARIANT_MMA_TW) {
-        plan.variant = SGEMM_VARIANT_MMA_T;
-        plan.ctas_per_sm = 0;
-    }
-    sgemm_status_t s = sgemm_plan_check(&plan, M, N, K);
+    sgemm_plan_t plan;
+    sgemm_status_t s = sgemm_splitk_noalloc_plan(N, K, M, split_k, nullptr, &plan);
     if (s != SGEMM_OK) return s;
     const sk::KernelInfo *ki = find(M, plan);
     if (!ki) return SGEMM_ERR_UNSUPPORTED_SHAPE;
 
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     DeviceSetup *st = nullptr;
-    s = setup_current_device(&st);
+    s = setup_current_device(cs, ki->fn, &st);
     if (s != SGEMM_OK) return s;
 
     const int kps = sk::split_kps(K, split_k);
@@ -159,17 +185,18 @@ extern "C" sgemm_status_t sgemm_bf16_skinny_splitk_noalloc(
     prm.split = split_k;
     prm.row_groups = sk::work_units(plan, N);
 
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, ki->fn, plan.threads, smem) !=
-            cudaSuccess ||
-        occ < 1)
+    // CTAs per SM as the regular path sizes them: the plan's, else the occupancy
+    int occ = plan.ctas_per_sm;
+    if (occ < 1 &&
+        (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, ki->fn, plan.threads, smem) !=
+             cudaSuccess ||
+         occ < 1))
         occ = 1;
     const long long need = sk::ctas_wanted(plan, N);
     long long slots = static_cast<long long>(st->sms) * occ / split_k;
     if (slots < 1) slots = 1;
     const int grid_x = static_cast<int>(need < slots ? need : slots);
 
-    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid_x), static_cast<unsigned>(split_k), 1);
     cfg.blockDim = dim3(static_cast<unsigned>(plan.threads), 1, 1);

@@ -45,8 +45,6 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 DEFAULT_OUT = os.path.join(HERE, "csrc", "plan_table.inc")
 
 
-# bulk-copy kernel geometry: (stage width in 32-element k-blocks, ring slots)
-BULK_GEOMETRY = [(16, 8), (32, 4), (32, 6), (64, 2), (64, 3)]
 # warp-owned-tile tensor-core kernel: warps sharing a tile's K range x CTAs per SM
 TW_SPLITS = [1, 2, 4, 8]
 TW_CTAS = [0, 1, 2]
@@ -57,13 +55,13 @@ TC05_SPLITS = [1, 2, 3, 4, 6, 8, 16]
 TC05_CTAS = [0, 1, 2]
 
 
-def candidates(M, N, K, splits):
+def candidates(M, N, K, splits, ctas=(0,)):
+    """Every compiled plan x split (and x CTAs per SM of the grid, `ctas`; 0 =
+    the occupancy limit) that can run (M, N, K)."""
     out = []
     for i in range(sk.sgemm_plan_count()):
         base = sk.sgemm_plan_get(i)
-        if base.variant == sk.SGEMM_VARIANT_BULK:
-            variants = [base.copy(k_unroll=kb, stages=ring) for kb, ring in BULK_GEOMETRY]
-        elif base.variant == sk.SGEMM_VARIANT_MMA_TW:
+        if base.variant == sk.SGEMM_VARIANT_MMA_TW:
             variants = [base.copy(split_k=s, ctas_per_sm=c) for s in TW_SPLITS for c in TW_CTAS]
         elif base.variant == sk.SGEMM_VARIANT_TC05:
             if base.k_unroll != 1:
@@ -72,7 +70,7 @@ def candidates(M, N, K, splits):
                         for r, nb in TC05_GEOMETRY for s in TC05_SPLITS
                         for c in (TC05_CTAS if s == 1 else [0])]
         else:
-            variants = [base.copy(split_k=s) for s in splits]
+            variants = [base.copy(split_k=s, ctas_per_sm=c) for s in splits for c in ctas]
         for p in variants:
             if sk.sgemm_plan_check(p, M, N, K) == sk.SGEMM_OK:
                 out.append(p)
@@ -80,7 +78,7 @@ def candidates(M, N, K, splits):
 
 
 def sweep_shape(N, K, Ms, splits, flags, trials, replays, min_bytes, pair=False, log=print,
-                prefilter=0, prefilter_bytes=0.0):
+                prefilter=0, prefilter_bytes=0.0, ctas=(0,)):
     """Time every candidate plan of (N, K) for each M; returns {M: result}.
 
     prefilter = P > 0 times the candidates in two stages: first all of them on
@@ -108,7 +106,7 @@ def sweep_shape(N, K, Ms, splits, flags, trials, replays, min_bytes, pair=False,
     for M in Ms:
         x = synth.normal_bf16((R, M, K), synth.X_STD, seed=1000 + M, device=dev)
         y = torch.empty((R, M, N), dtype=torch.bfloat16, device=dev)
-        cands = candidates(M, N, K, splits)
+        cands = candidates(M, N, K, splits, ctas)
         heur = sk.sgemm_plan_select(N, K, M)
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
@@ -236,6 +234,9 @@ def main(argv=None):
     ap.add_argument("--json", default=None, help="also write all timings here")
     ap.add_argument("--ms", default="1,2,3,4")
     ap.add_argument("--splits", default="1,2,4")
+    ap.add_argument("--ctas", default="0",
+                    help="CTAs per SM of the grid for the streaming and mma.sync plans "
+                         "(0 = occupancy limit), e.g. 0,1,2")
     ap.add_argument("--trials", type=int, default=5)
     ap.add_argument("--replays", type=int, default=10)
     ap.add_argument("--min-bytes", type=float, default=float(1 << 30))
@@ -255,6 +256,7 @@ def main(argv=None):
     min_bytes = max(args.min_bytes, 4 * l2)
     Ms = [int(v) for v in args.ms.split(",")]
     splits = [int(v) for v in args.splits.split(",")]
+    ctas = tuple(int(v) for v in args.ctas.split(","))
     flags = sk.SGEMM_FLAG_PDL | sk.SGEMM_FLAG_WEIGHTS_READONLY
     shapes = DECODE_SHAPES
     if args.shapes:
@@ -265,14 +267,14 @@ def main(argv=None):
         entries = read_table(args.merge)
     for (N, K) in shapes:
         res = sweep_shape(N, K, Ms, splits, flags, args.trials, args.replays, min_bytes,
-                          prefilter=args.prefilter, prefilter_bytes=2 * l2)
+                          prefilter=args.prefilter, prefilter_bytes=2 * l2, ctas=ctas)
         for M, r in res.items():
             entries[(N, K, M)] = r
             dump[f"{N}x{K}x{M}"] = r
     if not args.no_pair:
         N, K = PAIR_SHAPE
         res = sweep_shape(N, K, Ms, splits, flags, args.trials, args.replays, min_bytes, pair=True,
-                          prefilter=args.prefilter, prefilter_bytes=2 * l2)
+                          prefilter=args.prefilter, prefilter_bytes=2 * l2, ctas=ctas)
         for M, r in res.items():
             entries[(N, K, M)] = r
             dump[f"{N}x{K}x{M}-pair"] = r

@@ -106,13 +106,8 @@ enum {
                                      of W as the B operand: 8-row tiles, each lane streams 16 B of
                                      one row per step.  rows_per_warp = 8, lanes_per_row = 4,
                                      k_unroll = k-blocks per batch, stages = 1 or 2 batches */
-    SGEMM_VARIANT_BULK = 4,       /* one persistent CTA per SM streams a balanced row range of W
-                                     with cp.async.bulk copies into an mbarrier-tracked ring of
-                                     shared-memory slots (a producer thread), consumer warps run
-                                     the x-as-A MMA on it.  threads = 32 * (1 + consumer warps),
-                                     rows_per_warp = 8, lanes_per_row = 4, k_unroll = stage width
-                                     in 32-element k-blocks, stages = ring slots (2..16),
-                                     split_k = 1 */
+    /* 4: retired (a bulk-copy kernel that no sweep ever selected); plans with
+       variant 4 are refused with SGEMM_ERR_UNSUPPORTED_SHAPE */
     SGEMM_VARIANT_LDG_FFMA2 = 5,  /* the streaming kernel of variant 0 with packed FP32x2 FMA
                                      (two partial sums per output, even and odd k, added at the
                                      end): half the FMA instructions */
@@ -168,10 +163,10 @@ enum {
  *   kernel finishes. */
 #define SGEMM_FLAG_PDL 1u
 #define SGEMM_FLAG_WEIGHTS_READONLY 2u
-/* TEST ONLY: the kernels that wait on mbarriers for copies (SGEMM_VARIANT_BULK
- * and SGEMM_VARIANT_TC05) issue no copies, so their bounded waits run out
- * (about 0.2 s each); they then write NaN outputs, set the device error word
- * and return.  Exercises failure detection without a fault.  Other variants
+/* TEST ONLY: the kernel that waits on mbarriers for its copies
+ * (SGEMM_VARIANT_TC05) issues no copies, so its bounded waits run out (about
+ * 0.2 s each); it then writes NaN outputs, sets the device error word and
+ * returns.  Exercises failure detection without a fault.  Other variants
  * ignore the flag. */
 #define SGEMM_FLAG_TEST_STALL 4u
 
@@ -244,13 +239,6 @@ sgemm_status_t sgemm_plan_check(const sgemm_plan_t *plan, int M, int N, int K);
  * streams must be ordered by the caller. */
 sgemm_status_t sgemm_init(void);
 
-/* The elementwise step between consecutive GEMMs of a decode chain (vLLM PR
- * #65306, Validation: the chain's GEMMs are separated by a short elementwise
- * kernel):
- *     x[k] = RNE_bf16( float(y[k mod n_src]) * scale )   for 0 <= k < n_dst.
- * y and x are DEVICE arrays of BF16 bits (2-byte aligned, not overlapping).
- * flags: SGEMM_FLAG_PDL launches it as a programmatic dependent (it waits for
- * the previous kernel before reading y).  Errors as for the GEMM calls. */
 /* One GEMM of a decode chain with that elementwise step fused into its
  * epilogue: y = x . W^T as sgemm_bf16_skinny_ex (same plan, same bits), and
  *     x_next[m][k] = RNE_bf16( float(y[m][k mod N]) * scale )  for 0 <= k < n_next
@@ -282,6 +270,13 @@ sgemm_status_t sgemm_bf16_skinny_f32out_ex(const sgemm_bf16_t *x, long long ldx,
                                            int N, int K, const sgemm_plan_t *plan, unsigned flags,
                                            sgemm_stream_t stream);
 
+/* The elementwise step between consecutive GEMMs of a decode chain (vLLM PR
+ * #65306, Validation: the chain's GEMMs are separated by a short elementwise
+ * kernel):
+ *     x[k] = RNE_bf16( float(y[k mod n_src]) * scale )   for 0 <= k < n_dst.
+ * y and x are DEVICE arrays of BF16 bits (2-byte aligned, not overlapping).
+ * flags: SGEMM_FLAG_PDL launches it as a programmatic dependent (it waits for
+ * the previous kernel before reading y).  Errors as for the GEMM calls. */
 sgemm_status_t sgemm_bf16_rescale(const sgemm_bf16_t *y, long long n_src, sgemm_bf16_t *x,
                                   long long n_dst, float scale, unsigned flags,
                                   sgemm_stream_t stream);
@@ -295,20 +290,19 @@ sgemm_status_t sgemm_bf16_rescale(const sgemm_bf16_t *y, long long n_src, sgemm_
  * plugins or embedded runtimes that may not grow their footprint after
  * start-up, latency-critical loops where a possibly synchronizing cudaMalloc
  * is not allowed).  It computes y = x . W^T exactly like sgemm_bf16_skinny_ex
- * with the selected plan and split_k splits (bitwise-equal results), but keeps
- * the FP32 partial sums in a fixed, library-owned device array of
- * SGEMM_NOALLOC_SCRATCH_BYTES (4 MiB) instead of allocated scratch.
+ * with the plan sgemm_splitk_noalloc_plan(N, K, M, split_k, NULL, ...) returns
+ * (bitwise-equal results), but keeps the FP32 partial sums in a fixed,
+ * library-owned device array of SGEMM_NOALLOC_SCRATCH_BYTES (4 MiB) instead
+ * of allocated scratch.
  * - The caller passes inputs and outputs as for sgemm_bf16_skinny_ex (device
- *   pointers, strides in elements); split_k must be >= 2.  The selected plan
- *   is used with split_k splits; when the selected plan cannot split K across
- *   CTAs (the bulk-copy variant), a CUDA-core streaming plan is used instead,
- *   and a warp-owned-tile plan (SGEMM_VARIANT_MMA_TW) runs as the x-as-A
- *   tensor-core plan with the same unroll (SGEMM_VARIANT_MMA_T).
+ *   pointers, strides in elements); split_k must be >= 2.  The launch is
+ *   plain (no launch flags).
  * - split_k * M * N * 4 bytes must fit SGEMM_NOALLOC_SCRATCH_BYTES; larger
  *   problems return SGEMM_ERR_UNSUPPORTED_SHAPE and launch nothing.
  * - The first call on a device does a one-time set-up with that device current
- *   (it looks up the array's device address and sets kernel attributes).
- *   Make that first call before any stream capture.
+ *   (it looks up the array's device address).  That first call must come
+ *   before any stream capture: made on a capturing stream it returns
+ *   SGEMM_ERR_INVALID_ARG and enqueues nothing.  Later calls may be captured.
  * - The array lives in every GPU that loads the library until the process
  *   exits.  All calls on a device share it and it keeps what the last call
  *   left; nothing in it needs clearing, because each call writes every partial
@@ -320,9 +314,23 @@ sgemm_status_t sgemm_bf16_skinny_splitk_noalloc(const sgemm_bf16_t *x, long long
                                                 long long ldy, int M, int N, int K, int split_k,
                                                 sgemm_stream_t stream);
 
+/* The plan sgemm_bf16_skinny_splitk_noalloc runs for (N, K, M, split_k): the
+ * plan `selected` (NULL = sgemm_plan_select(N, K, M)) with split_k K splits
+ * through scratch memory and a second-pass reduce.  Plans that do not split K
+ * that way are replaced: a TMA + tcgen05 plan (SGEMM_VARIANT_TC05, whose split
+ * reduces inside a cluster) by the CUDA-core streaming plan (variant
+ * SGEMM_VARIANT_LDG_MIXFMA, 256 threads, 1 row per warp, 32 lanes per row,
+ * k_unroll 8, 1 stage); a warp-owned-tile plan (SGEMM_VARIANT_MMA_TW) by the
+ * x-as-A plan with CTA-wide tiles (SGEMM_VARIANT_MMA_T) with the same stages
+ * and k_unroll capped at 8, ctas_per_sm 0.  Pure host function.  Writes *out
+ * and returns sgemm_plan_check of it for (M, N, K); SGEMM_ERR_INVALID_ARG for
+ * a NULL out or split_k < 2. */
+sgemm_status_t sgemm_splitk_noalloc_plan(int N, int K, int M, int split_k,
+                                         const sgemm_plan_t *selected, sgemm_plan_t *out);
+
 /* Reads and clears the device error word of the current device: bit 0 is set
- * when a kernel gave up a bounded wait for its data (SGEMM_VARIANT_BULK or
- * SGEMM_VARIANT_TC05; the outputs of that launch were written as NaN).
+ * when a kernel gave up a bounded wait for its data (SGEMM_VARIANT_TC05; the
+ * outputs of that launch were written as NaN).
  * *flags = 0 when nothing went wrong.  The word is a static device variable
  * of the library (no allocation).  Synchronous (waits for the device); do not
  * call during stream capture. */

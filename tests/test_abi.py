@@ -139,7 +139,7 @@ def test_batched_argument_checks(lib):
 def test_bad_plans_rejected(lib):
     good = sk.sgemm_plan_select(4096, 4096, 1)
     assert sk.sgemm_plan_check(good, 1, 4096, 4096) == sk.SGEMM_OK
-    for change in ({"variant": 7}, {"variant": -1}, {"threads": 48}, {"threads": 512}, {"vec_bytes": 8},
+    for change in ({"variant": 7}, {"variant": -1}, {"variant": 4}, {"threads": 48}, {"threads": 512}, {"vec_bytes": 8},
                    {"split_k": 0}, {"k_unroll": 3}, {"lanes_per_row": 4}, {"stages": 3}):
         bad = good.copy(**change)
         assert sk.sgemm_plan_check(bad, 1, 4096, 4096) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE, change
@@ -187,12 +187,12 @@ def test_plan_select_out_of_range_still_returns_a_plan(lib):
 
 
 def test_heuristic_plan_splits_k_when_rows_leave_sms_idle(lib):
-    # (288, 4096) at M = 1..4 has no table entry: 36 CTAs of rows alone would
+    # (320, 4096) at M = 1..4 has no table entry: 40 CTAs of rows alone would
     # leave most of 152 SMs idle, so K is split (down to 512 elements a split)
     for M in (1, 2, 3, 4):
-        p = sk.sgemm_plan_select(288, 4096, M)
+        p = sk.sgemm_plan_select(320, 4096, M)
         assert p.id == -1 and p.split_k >= 4, p
-        assert sk.sgemm_plan_check(p, M, 288, 4096) == sk.SGEMM_OK
+        assert sk.sgemm_plan_check(p, M, 320, 4096) == sk.SGEMM_OK
     # enough rows: no extra split
     assert sk.sgemm_plan_select(100000, 4096, 1).split_k == 1
     # M >= 5 without a table entry: the 16-row tensor-core kernel
@@ -254,3 +254,40 @@ def test_plan_table_round_trip(tmp_path):
     for k in entries:
         assert again[k]["plan"] == entries[k]["plan"]
         assert abs(again[k]["us"] - entries[k]["us"]) < 1e-3
+
+
+def test_noalloc_plan_substitutions(lib):
+    """The plan the no-allocation split-K call runs: the selected plan with the
+    requested split, except for plans that do not split K through scratch."""
+    def kernel(variant, **kw):
+        for i in range(sk.sgemm_plan_count()):
+            p = sk.sgemm_plan_get(i)
+            if p.variant == variant and all(getattr(p, k) == v for k, v in kw.items()):
+                return p
+        raise AssertionError((variant, kw))
+
+    # an ordinary streaming plan keeps everything but split_k
+    base = kernel(sk.SGEMM_VARIANT_LDG_MIXFMA)
+    st, p = sk.sgemm_splitk_noalloc_plan(4096, 4096, 2, 3, base)
+    assert st == sk.SGEMM_OK and p.as_dict() == base.copy(split_k=3).as_dict()
+    # tcgen05 plans (their split reduces in a cluster) -> the CUDA-core streaming plan
+    st, p = sk.sgemm_splitk_noalloc_plan(4096, 4096, 4, 4, kernel(sk.SGEMM_VARIANT_TC05))
+    assert st == sk.SGEMM_OK
+    assert (p.variant, p.threads, p.rows_per_warp, p.lanes_per_row, p.k_unroll, p.stages,
+            p.split_k) == (sk.SGEMM_VARIANT_LDG_MIXFMA, 256, 1, 32, 8, 1, 4), p
+    # warp-owned tiles -> CTA-wide x-as-A tiles, the unroll capped at 8 (U = 16 exists
+    # only in the warp-owned form)
+    tw16 = kernel(sk.SGEMM_VARIANT_MMA_TW, k_unroll=16).copy(ctas_per_sm=2)
+    st, p = sk.sgemm_splitk_noalloc_plan(4096, 4096, 4, 2, tw16)
+    assert st == sk.SGEMM_OK, p
+    assert (p.variant, p.k_unroll, p.stages, p.split_k, p.ctas_per_sm) == \
+        (sk.SGEMM_VARIANT_MMA_T, 8, tw16.stages, 2, 0), p
+    for tw in (kernel(sk.SGEMM_VARIANT_MMA_TW, k_unroll=u, stages=s)
+               for u, s in ((4, 1), (8, 1), (16, 1), (2, 2), (4, 2), (8, 2))):
+        for M in (1, 4, 8):
+            st, p = sk.sgemm_splitk_noalloc_plan(4096, 4096, M, 2, tw)
+            assert st == sk.SGEMM_OK, (tw, p)
+    # the selected plan by default; split_k below 2 is refused
+    st, p = sk.sgemm_splitk_noalloc_plan(4096, 8192, 1, 4)
+    assert st == sk.SGEMM_OK and p.split_k == 4
+    assert sk.sgemm_splitk_noalloc_plan(4096, 8192, 1, 1)[0] == sk.SGEMM_ERR_INVALID_ARG

@@ -92,10 +92,8 @@ def test_every_plan_every_split(M, split):
     for p in _all_plans():
         plan = p.copy(split_k=split)
         if sk.sgemm_plan_check(plan, M, N, K) != sk.SGEMM_OK:
-            # the bulk kernel refuses splits; the warp-owned-tile kernel splits K
-            # inside a CTA, 1, 2, 4 or 8 ways
-            assert (p.variant == sk.SGEMM_VARIANT_BULK and split > 1) or \
-                (p.variant == sk.SGEMM_VARIANT_MMA_TW and split in (3, 5))
+            # the warp-owned-tile kernel splits K inside a CTA, 1, 2, 4 or 8 ways
+            assert p.variant == sk.SGEMM_VARIANT_MMA_TW and split in (3, 5)
             continue
         y = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=plan)
         torch.cuda.synchronize()
@@ -336,8 +334,9 @@ def test_plans_with_same_lanes_per_row_agree_bitwise(M):
     lanes per row, FMA pairing): the mixed-precision FMA and the widened FP32
     FMA, any R, U and CTA size must give the same bits (and so must any packed
     FP32x2 plans among themselves, and any diagonal-MMA plans among
-    themselves).  For the tensor-core and bulk kernels it depends on (K range,
-    warps per CTA): any U and batch depth must give the same bits."""
+    themselves).  For the mma.sync kernels it depends on (K range, warps per
+    CTA), for the tcgen05 kernel on (K range, split): any U, batch depth and
+    ring must give the same bits."""
     N, K = 1500, 3072
     x, W = _inputs(M, N, K, seed=31)
     xd, Wd = x.to(DEV), W.to(DEV)
@@ -350,8 +349,7 @@ def test_plans_with_same_lanes_per_row_agree_bitwise(M):
             y = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=plan)
             torch.cuda.synchronize()
             mma = plan.variant in (sk.SGEMM_VARIANT_MMA, sk.SGEMM_VARIANT_MMA_T,
-                                   sk.SGEMM_VARIANT_BULK, sk.SGEMM_VARIANT_MMA_TW,
-                                   sk.SGEMM_VARIANT_TC05)
+                                   sk.SGEMM_VARIANT_MMA_TW, sk.SGEMM_VARIANT_TC05)
             # the widened and the mixed-precision FMA round identically; the packed
             # FP32x2 FMA keeps two partial sums, a different order of its own
             ffma2 = plan.variant in (sk.SGEMM_VARIANT_LDG_FFMA2, sk.SGEMM_VARIANT_LDGX_FFMA2)
@@ -406,65 +404,6 @@ def test_pdl_chain_matches_plain_launches(flags, split):
     torch.cuda.synchronize()
     for a, b in zip(ref, gout):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
-
-
-# ----------------------------------------------------- bulk-copy pipeline plans
-def _bulk_plan(threads=288, stage_blocks=32, ring=4):
-    for p in _all_plans():
-        if p.variant == sk.SGEMM_VARIANT_BULK:
-            return p.copy(threads=threads, k_unroll=stage_blocks, stages=ring)
-    raise AssertionError("no bulk plan compiled")
-
-
-@pytest.mark.parametrize("N,K", [(1, 8), (5, 1000), (300, 1024), (1001, 4096), (777, 2600),
-                                 (4096, 8192), (2049, 128)])
-@pytest.mark.parametrize("M", [1, 2, 3, 4])
-def test_bulk_plan_shapes(M, N, K):
-    x, W = _inputs(M, N, K, seed=1300 + N + K)
-    plan = _bulk_plan()
-    assert sk.sgemm_plan_check(plan, M, N, K) == sk.SGEMM_OK
-    y = sk.sgemm_bf16_skinny_ex(x.to(DEV), W.to(DEV), plan=plan)
-    torch.cuda.synchronize()
-    _check(x, W, y)
-
-
-@pytest.mark.parametrize("threads,stage_blocks,ring", [(160, 8, 2), (160, 16, 8), (288, 64, 3),
-                                                      (288, 16, 16), (96, 32, 4)])
-def test_bulk_ring_and_stage_geometry(threads, stage_blocks, ring):
-    M, N, K = 4, 1203, 3080  # ragged rows, K not a multiple of the stage width or of 32
-    x, W = _inputs(M, N, K, seed=1400 + ring)
-    plan = _bulk_plan(threads, stage_blocks, ring)
-    y = sk.sgemm_bf16_skinny_ex(x.to(DEV), W.to(DEV), plan=plan,
-                                flags=sk.SGEMM_FLAG_PDL | sk.SGEMM_FLAG_WEIGHTS_READONLY)
-    torch.cuda.synchronize()
-    _check(x, W, y)
-    flags = sk.sgemm_device_errors()
-    assert flags == 0
-
-
-def test_bulk_batched_and_deterministic():
-    M, N, K = 3, 4096, 128
-    plan = _bulk_plan(160, 4, 8)
-    items, refs = [], []
-    for i in range(2):
-        x, W = _inputs(M, N, K, seed=1500 + i, wstd=synth.PAIR_W_STD)
-        items.append((x.to(DEV), W.to(DEV)))
-        refs.append((x, W))
-    a = sk.sgemm_bf16_skinny_batched_ex(items, plan=plan)
-    b = sk.sgemm_bf16_skinny_batched_ex(items, plan=plan)
-    torch.cuda.synchronize()
-    for (x, W), ya, yb in zip(refs, a, b):
-        assert torch.equal(ya.view(torch.int16), yb.view(torch.int16))
-        _check(x, W, ya)
-
-
-def test_bulk_rejects_split_k_and_oversized_rings():
-    plan = _bulk_plan()
-    assert sk.sgemm_plan_check(plan.copy(split_k=2), 1, 4096, 4096) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE
-    assert sk.sgemm_plan_check(plan.copy(stages=17), 1, 4096, 4096) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE
-    # 16 slots of 8 x 2048 BF16 rows do not fit in shared memory
-    assert sk.sgemm_plan_check(plan.copy(k_unroll=64, stages=16), 1, 4096, 4096) == \
-        sk.SGEMM_ERR_UNSUPPORTED_SHAPE
 
 
 # ------------------------------------------- warp-owned-tile tensor-core plans
