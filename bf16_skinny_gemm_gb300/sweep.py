@@ -12,7 +12,13 @@ at least 1 GiB, captured in a CUDA graph, trials interleaved):
   CTA size x split factor): one CUDA graph of R GEMMs through the public
   ``sgemm_bf16_skinny_ex`` call, launched with the decode-chain launch flags
   (programmatic dependent launch, weights read-only);
-- T trials of P replays each, interleaved across candidates; the score is the
+- T trials of P replays each, interleaved across candidates; before every
+  timed replay a separate buffer of several GiB is read, so each replay starts
+  from the state a decode step leaves behind (caches and address translations
+  filled by other data; a clean read, so nothing is written back during the
+  timed replay).  Replaying one graph back to back instead lets part of the
+  weight set and its translations survive from the previous replay, which
+  flatters the CUDA-core streaming kernels by about 10 %.  The score is the
   median per-GEMM time.  The fastest candidate is kept.  (The pages keep a
   plan only if it beats cuBLAS by 5 %; here there is no other library to fall
   back to, so the table keeps the fastest plan outright.)
@@ -78,15 +84,13 @@ def candidates(M, N, K, splits, ctas=(0,)):
 
 
 def sweep_shape(N, K, Ms, splits, flags, trials, replays, min_bytes, pair=False, log=print,
-                prefilter=0, prefilter_bytes=0.0, ctas=(0,)):
+                prefilter=0, prefilter_bytes=0.0, ctas=(0,), cold=None):
     """Time every candidate plan of (N, K) for each M; returns {M: result}.
 
-    prefilter = P > 0 times the candidates in two stages: first all of them on
-    a shorter chain (weight copies totalling ``prefilter_bytes``, still at least
-    twice L2 so every GEMM reads HBM) with 2 trials x 5 replays, then the P
-    fastest (and the heuristic plan) with the full protocol; the winner comes
-    from the second stage.  This cuts the graph captures that dominate the
-    sweep's time for small weights.
+    prefilter = P > 0 times the candidates in two stages: first all of them
+    (weight copies totalling ``prefilter_bytes``) with 2 trials x 3 replays,
+    then the P fastest (and the heuristic plan) with the full protocol; the
+    winner comes from the second stage.
     """
     dev = torch.device("cuda")
     R = max(2, math.ceil(min_bytes / (2 * N * K)))
@@ -138,17 +142,30 @@ def sweep_shape(N, K, Ms, splits, flags, trials, replays, min_bytes, pair=False,
                 g.replay()
             torch.cuda.synchronize()
             times = [[] for _ in plans]
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
             per_launch = n // 2 if pair else n
             for _ in range(n_trials):
                 for ci, g in enumerate(graphs):
-                    e0.record()
+                    if cold is None:  # back-to-back replays
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record()
+                        for _ in range(n_replays):
+                            g.replay()
+                        e1.record()
+                        e1.synchronize()
+                        times[ci].append(e0.elapsed_time(e1) * 1e3 / n_replays / per_launch)
+                        continue
+                    evs = []
                     for _ in range(n_replays):
+                        cold.sum()  # not timed: caches and translations now hold other data
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record()
                         g.replay()
-                    e1.record()
-                    e1.synchronize()
-                    times[ci].append(e0.elapsed_time(e1) * 1e3 / n_replays / per_launch)
+                        e1.record()
+                        evs.append((e0, e1))
+                    torch.cuda.synchronize()
+                    times[ci] += [a.elapsed_time(b) * 1e3 / per_launch for a, b in evs]
             del graphs
             torch.cuda.synchronize()
             return [statistics.median(t) for t in times]
@@ -157,7 +174,7 @@ def sweep_shape(N, K, Ms, splits, flags, trials, replays, min_bytes, pair=False,
         if prefilter > 0 and len(cands) > prefilter:
             R1 = min(R, max(2, math.ceil(prefilter_bytes / (2 * N * K))))
             R1 += R1 % 2 if pair else 0
-            med1 = time_plans(cands, R1, 2, 5)
+            med1 = time_plans(cands, R1, 2, 3)
             keep = sorted(range(len(cands)), key=lambda i: med1[i])[:prefilter]
             keep += [i for i, p in enumerate(cands) if same(p, heur) and i not in keep]
             stage1 = [(cands[i].as_dict(), round(med1[i], 3)) for i in
@@ -234,6 +251,9 @@ def main(argv=None):
     ap.add_argument("--json", default=None, help="also write all timings here")
     ap.add_argument("--ms", default="1,2,3,4")
     ap.add_argument("--splits", default="1,2,4")
+    ap.add_argument("--cold-gib", type=float, default=4.0,
+                    help="GiB of other memory read before each timed replay (0 = replay "
+                         "back to back)")
     ap.add_argument("--ctas", default="0",
                     help="CTAs per SM of the grid for the streaming and mma.sync plans "
                          "(0 = occupancy limit), e.g. 0,1,2")
@@ -257,6 +277,9 @@ def main(argv=None):
     Ms = [int(v) for v in args.ms.split(",")]
     splits = [int(v) for v in args.splits.split(",")]
     ctas = tuple(int(v) for v in args.ctas.split(","))
+    cold = None
+    if args.cold_gib > 0:
+        cold = torch.ones(int(args.cold_gib * 2**30) // 8, dtype=torch.int64, device="cuda")
     flags = sk.SGEMM_FLAG_PDL | sk.SGEMM_FLAG_WEIGHTS_READONLY
     shapes = DECODE_SHAPES
     if args.shapes:
@@ -267,21 +290,26 @@ def main(argv=None):
         entries = read_table(args.merge)
     for (N, K) in shapes:
         res = sweep_shape(N, K, Ms, splits, flags, args.trials, args.replays, min_bytes,
-                          prefilter=args.prefilter, prefilter_bytes=2 * l2, ctas=ctas)
+                          prefilter=args.prefilter, prefilter_bytes=min_bytes, ctas=ctas,
+                          cold=cold)
         for M, r in res.items():
             entries[(N, K, M)] = r
             dump[f"{N}x{K}x{M}"] = r
     if not args.no_pair:
         N, K = PAIR_SHAPE
         res = sweep_shape(N, K, Ms, splits, flags, args.trials, args.replays, min_bytes, pair=True,
-                          prefilter=args.prefilter, prefilter_bytes=2 * l2, ctas=ctas)
+                          prefilter=args.prefilter, prefilter_bytes=min_bytes, ctas=ctas,
+                          cold=cold)
         for M, r in res.items():
             entries[(N, K, M)] = r
             dump[f"{N}x{K}x{M}-pair"] = r
     note = (f"{torch.cuda.get_device_name(0)}, {len(entries)} entries, cold L2 (>= "
-            f"{min_bytes / 2**30:.2f} GiB of weight copies per shape), launch flags PDL|readonly, "
+            f"{min_bytes / 2**30:.2f} GiB of weight copies per shape"
+            + (f", {args.cold_gib:g} GiB of other memory read before each timed replay"
+               if cold is not None else ", replays back to back")
+            + f"), launch flags PDL|readonly, "
             f"{args.trials} interleaved trials x {args.replays} graph replays, median"
-            + (f", top {args.prefilter} of a shorter cold chain (>= 2 x L2) timed fully"
+            + (f", top {args.prefilter} of a first pass (2 trials x 3 replays) timed fully"
                if args.prefilter else ""))
     write_table(entries, args.out, note)
     if args.json:
