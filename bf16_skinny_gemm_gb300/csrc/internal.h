@@ -51,7 +51,7 @@ struct Params {
 // Kernel parameters of the TMA + tcgen05 kernel (skinny_tc05.cuh): the common
 // parameters plus one pair of tensor maps (W and x) per problem, which the
 // copy engine reads from the kernel's parameter space.  About 2.6 KB.
-struct alignas(64) Tc05Params {
+struct Tc05Params {
     CUtensorMap tw[kMaxBatch];  // W [N][K]: dims {K, N}, box {64, 128}, 128-byte swizzle
     CUtensorMap tx[kMaxBatch];  // x [M][K] (row stride ldx): dims {K, M}, box {64, 16}
     Params base;                // y, strides, epilogue, flags, error word (ws unused)
