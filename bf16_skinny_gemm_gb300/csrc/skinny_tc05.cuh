@@ -279,23 +279,22 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
     const bool early_w = !pdl || (bp.flags & kFlagWeightsReadOnly);
     const int pre = early_w ? min(S, total) : 0;
 
-    if (threadIdx.x == 0) {
-        prefetch_tmap(tw);
-        prefetch_tmap(tx);
-        abort_flag = 0;
-        for (int s = 0; s < S; ++s) {
-            bar_init(full0 + 8 * s, 1);
-            bar_init(empty0 + 8 * s, 1);
+    if (warp == 0) {
+        // The lanes of warp 0 set up the mbarriers in parallel, then each issues one stage
+        // of the first ring of W, before the tensor-memory allocation and the CTA barrier.
+        // (One thread doing all of it took about 2 us from kernel entry to the last copy
+        // of an 8-stage ring: each copy costs its issuing thread about 0.1-0.2 us.)
+        if (lane == 0) {
+            prefetch_tmap(tw);
+            prefetch_tmap(tx);
+            abort_flag = 0;
         }
-        bar_init(accf0, 1);
-        bar_init(accf0 + 8, 1);
-        bar_init(acce0, 4);
-        bar_init(acce0 + 8, 4);
-        bar_init(fin, 1);
+        for (int i = lane; i < 2 * S; i += 32) bar_init(full0 + 8 * i, 1);  // full[S], empty[S]
+        if (lane < 5) bar_init(accf0 + 8 * lane, (lane == 2 || lane == 3) ? 4 : 1);  // accf, acce, fin
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the copy engine
-        // the first loads go out before the tensor-memory allocation and the CTA barrier
-        for (int g = 0; g < pre; ++g) issue_w(g);
+        __syncwarp();
+        for (int g = lane; g < pre; g += 32) issue_w(g);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -317,9 +316,12 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
     int issued = 0;  // stages the producer issued
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
-        if (lane == 0 && total > 0) {
+        if (total > 0) {
             if (pdl) pdl_wait();
-            for (int g = 0; g < pre; ++g) issue_x(g);
+            for (int g = lane; g < pre; g += 32) issue_x(g);  // the first ring's x, one stage per lane
+            __syncwarp();
+        }
+        if (lane == 0 && total > 0) {
             issued = pre;
             for (int g = pre; g < total; ++g) {
                 const int slot = g % S;
