@@ -88,17 +88,54 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
 //    chain's GEMMs, done on the value just rounded, so the result is bitwise
 //    that of the separate step.
 //  - FP32 output: y = v, no rounding.
-__device__ __forceinline__ void store_out(const Params &p, const Item &it, int m, int n, float v) {
-    if (p.out_f32) {
-        reinterpret_cast<float *>(it.y)[m * it.ldy + n] = v;
+// `Out` holds what the epilogue reads of the parameters.
+struct Out {
+    uint16_t *y;
+    uint16_t *xn;
+    long long ldy;
+    long long ldxn;
+    int out_f32;
+    int xn_len;
+    int N;
+    float xn_scale;
+};
+
+__device__ __forceinline__ Out out_of(const Params &p, const Item &it) {
+    return Out{it.y, it.xn, it.ldy, it.ldxn, p.out_f32, p.xn_len, p.N, p.xn_scale};
+}
+
+// The same, read into registers now: a kernel whose epilogue would first touch
+// these parameters at its very end (a constant-cache miss on the critical
+// path) reads them when it starts.  The moves are opaque, so the compiler
+// cannot sink the reads back to the use.
+__device__ __forceinline__ Out out_pinned(const Params &p, const Item &it) {
+    Out o = out_of(p, it);
+    asm volatile("mov.b64 %0, %0;" : "+l"(o.y));
+    asm volatile("mov.b64 %0, %0;" : "+l"(o.xn));
+    asm volatile("mov.b64 %0, %0;" : "+l"(o.ldy));
+    asm volatile("mov.b64 %0, %0;" : "+l"(o.ldxn));
+    asm volatile("mov.b32 %0, %0;" : "+r"(o.out_f32));
+    asm volatile("mov.b32 %0, %0;" : "+r"(o.xn_len));
+    asm volatile("mov.b32 %0, %0;" : "+r"(o.N));
+    asm volatile("mov.b32 %0, %0;" : "+f"(o.xn_scale));
+    return o;
+}
+
+__device__ __forceinline__ void store_out(const Out &o, int m, int n, float v) {
+    if (o.out_f32) {
+        reinterpret_cast<float *>(o.y)[m * o.ldy + n] = v;
         return;
     }
     const uint16_t b = f32_to_bf16_rn(v);
-    it.y[m * it.ldy + n] = b;
-    if (it.xn) {
-        const uint16_t q = f32_to_bf16_rn(__uint_as_float(static_cast<uint32_t>(b) << 16) * p.xn_scale);
-        for (int k = n; k < p.xn_len; k += p.N) it.xn[m * it.ldxn + k] = q;
+    o.y[m * o.ldy + n] = b;
+    if (o.xn) {
+        const uint16_t q = f32_to_bf16_rn(__uint_as_float(static_cast<uint32_t>(b) << 16) * o.xn_scale);
+        for (int k = n; k < o.xn_len; k += o.N) o.xn[m * o.ldxn + k] = q;
     }
+}
+
+__device__ __forceinline__ void store_out(const Params &p, const Item &it, int m, int n, float v) {
+    store_out(out_of(p, it), m, n, v);
 }
 
 // acc += lo(x)*lo(w), then acc += hi(x)*hi(w): BF16 operands, FP32 addend,

@@ -29,9 +29,11 @@
 //       range of 128-row tiles and walks each tile's whole K;
 //     - split > 1: the `split` CTAs of a thread-block cluster share one tile,
 //       each a contiguous range of K boxes.  At the end every CTA but rank 0
-//       stores its FP32 partial tile into rank 0's shared memory
-//       (distributed shared memory), a cluster barrier orders the stores, and
-//       rank 0 adds the partials in rank order and writes y.
+//       pushes its FP32 partial tile into rank 0's shared memory with
+//       st.async (distributed shared memory), each store counted in bytes on
+//       rank 0's reduction mbarrier, and exits; rank 0 waits for those bytes,
+//       adds the partials in rank order and writes y.  (A cluster barrier in
+//       place of the mbarrier cost about 0.5 us more per GEMM.)
 //
 // The accumulation order of an output depends on (K, boxes per split) only:
 // never on M (the columns of one MMA are independent), the ring depth, the
@@ -95,6 +97,20 @@ __device__ __forceinline__ void bar_expect_tx(uint32_t b, unsigned bytes) {
                  : "memory");
 }
 
+// As bar_try, with cluster-scope acquire: for a barrier that other CTAs of the
+// cluster complete with st.async.
+__device__ __forceinline__ bool bar_try_cluster(uint32_t b, unsigned parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(b), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool bar_try(uint32_t b, unsigned parity) {
     uint32_t ok;
     asm volatile(
@@ -113,6 +129,14 @@ __device__ __forceinline__ bool bar_wait(uint32_t b, unsigned parity) {
     if (bar_try(b, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!bar_try(b, parity)) {
+        if (static_cast<long long>(global_ns() - t0) > kWaitLimitNs) return false;
+    }
+    return true;
+}
+__device__ __forceinline__ bool bar_wait_cluster(uint32_t b, unsigned parity) {
+    if (bar_try_cluster(b, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!bar_try_cluster(b, parity)) {
         if (static_cast<long long>(global_ns() - t0) > kWaitLimitNs) return false;
     }
     return true;
@@ -182,11 +206,32 @@ __device__ __forceinline__ void cluster_arrive_release() {
 __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
-// Store v at CTA-local shared address `local` of the cluster's CTA `rank`.
-__device__ __forceinline__ void st_cluster_f32(uint32_t local, uint32_t rank, float v) {
+// The shared::cluster address of CTA-local shared address `local` in the
+// cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+    return remote;
+}
+// Asynchronous stores of 1, 2 or 4 words into another CTA's shared memory
+// (shared::cluster addresses); each completes its bytes on mbarrier `bar` there.
+__device__ __forceinline__ void st_async1(uint32_t dst, float a, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst),
+                 "r"(__float_as_uint(a)), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async2(uint32_t dst, float a, float b, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(
+                     dst),
+                 "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async4(uint32_t dst, float a, float b, float c, float d, uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
+        "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)), "r"(__float_as_uint(d)),
+        "r"(bar)
+        : "memory");
 }
 
 __device__ __forceinline__ int read_flag(const int *f) {
@@ -197,8 +242,8 @@ template <int M>
 __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_constant__ Tc05Params p) {
     static_assert(M >= 1 && M <= 8, "x rows fill the first M columns of the MMA");
     extern __shared__ uint8_t smem_raw[];
-    // full[S], empty[S], accumulator full[2], accumulator empty[2], MMAs done
-    __shared__ __align__(8) uint64_t bars[2 * kMaxRingSlots + 5];
+    // full[S], empty[S], accumulator full[2], accumulator empty[2], MMAs done, partials in
+    __shared__ __align__(8) uint64_t bars[2 * kMaxRingSlots + 6];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -207,7 +252,8 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
     const int S = p.ring;
     const int NB = p.nb;
     const int stage_bytes = NB * kBoxBytes;
-    float *red = reinterpret_cast<float *>(ring + S * stage_bytes);  // [split-1][M][128]
+    constexpr int RC = red_cols(M);
+    float *red = reinterpret_cast<float *>(ring + S * stage_bytes);  // [split-1][128][RC]
 
     const Params &bp = p.base;
     const int bi = blockIdx.y;  // problem of a batched call
@@ -243,6 +289,7 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
     const uint32_t accf0 = full0 + 8 * 2 * kMaxRingSlots;
     const uint32_t acce0 = accf0 + 16;
     const uint32_t fin = acce0 + 16;
+    const uint32_t redb = fin + 8;  // rank 0: the other ranks' partial tiles have landed
 
     // The producer is thread 0.  Its tensor maps, and the stage -> (rows, boxes) map.
     const CUtensorMap *tw = &p.tw[bi];
@@ -290,7 +337,8 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
             abort_flag = 0;
         }
         for (int i = lane; i < 2 * S; i += 32) bar_init(full0 + 8 * i, 1);  // full[S], empty[S]
-        if (lane < 5) bar_init(accf0 + 8 * lane, (lane == 2 || lane == 3) ? 4 : 1);  // accf, acce, fin
+        // accf[2], acce[2], fin, redb
+        if (lane < 6) bar_init(accf0 + 8 * lane, (lane == 2 || lane == 3) ? 4 : 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the copy engine
         __syncwarp();
@@ -314,6 +362,7 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
     for (int m = 0; m < M; ++m) v[m] = 0.0f;
 
     int issued = 0;  // stages the producer issued
+    Out o{};         // epilogue warps: the output parameters, in registers
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
         if (total > 0) {
@@ -379,6 +428,7 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
         }
     } else {
         // --------------------------------------------------------------- epilogue
+        o = out_pinned(bp, it);  // read the output parameters while the copies stream
         if (pdl) pdl_wait();  // y (and the fused next input) may be read by the previous kernel
         const int q = warp & 3;  // tensor-memory lane quarter this warp may access
         const int row = q * 32 + lane;
@@ -400,9 +450,9 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
             for (int m = 0; m < M; ++m) v[m] = good ? __uint_as_float(r[m]) : __int_as_float(0x7fc00000);
             if (split == 1) {
                 const int n = (t_begin + i) * kRows + row;
-                if (n < bp.N) {
+                if (n < o.N) {
 #pragma unroll
-                    for (int m = 0; m < M; ++m) store_out(bp, it, m, n, v[m]);
+                    for (int m = 0; m < M; ++m) store_out(o, m, n, v[m]);
                 }
             }
         }
@@ -410,26 +460,64 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
     __syncwarp();
 
     if (split > 1) {
-        // deterministic K reduction across the cluster: ranks 1.. store their partial
-        // tile into rank 0's shared memory, rank 0 adds them in rank order
-        cluster_wait_acquire();  // every CTA of the cluster has started
-        if (warp >= 2 && rank > 0 && ntile > 0) {
-            const int row = (warp & 3) * 32 + lane;
-#pragma unroll
-            for (int m = 0; m < M; ++m)
-                st_cluster_f32(saddr(red + ((rank - 1) * M + m) * kRows + row), 0u, v[m]);
-        }
-        cluster_arrive_release();
+        // Deterministic K reduction across the cluster.  Ranks 1.. push their partial tile
+        // into rank 0's shared memory with st.async, every byte counted on rank 0's mbarrier
+        // redb, and are done; rank 0 waits for all of them and adds the partials in rank
+        // order.  The only cluster barrier before this is the one that shows every CTA of
+        // the cluster has started (so redb exists), which is long past by now.
         cluster_wait_acquire();
-        if (warp >= 2 && rank == 0 && ntile > 0) {
+        if (warp >= 2 && ntile > 0) {
             const int row = (warp & 3) * 32 + lane;
-            const int n = t_begin * kRows + row;
-            if (n < bp.N) {
+            if (rank > 0) {
+                const uint32_t dst = cluster_addr(saddr(red + ((rank - 1) * kRows + row) * RC), 0u);
+                const uint32_t bar = cluster_addr(redb, 0u);
+                if constexpr (RC == 1) {
+                    st_async1(dst, v[0], bar);
+                } else if constexpr (RC == 2) {
+                    st_async2(dst, v[0], v[M > 1 ? 1 : 0], bar);
+                } else {
 #pragma unroll
-                for (int m = 0; m < M; ++m) {
-                    float s = v[m];
-                    for (int rr = 1; rr < split; ++rr) s += red[((rr - 1) * M + m) * kRows + row];
-                    store_out(bp, it, m, n, s);
+                    for (int c = 0; c < RC; c += 4)
+                        st_async4(dst + 4 * c, v[c], c + 1 < M ? v[min(c + 1, M - 1)] : 0.0f,
+                                  c + 2 < M ? v[min(c + 2, M - 1)] : 0.0f,
+                                  c + 3 < M ? v[min(c + 3, M - 1)] : 0.0f, bar);
+                }
+            } else {
+                if (warp == 2 && lane == 0)
+                    bar_expect_tx(redb, static_cast<unsigned>((split - 1) * kRows * RC * sizeof(float)));
+                const bool got = bar_wait_cluster(redb, 0);
+                if (!got) atomicExch(&abort_flag, 1);
+                const int n = t_begin * kRows + row;
+                if (n < o.N) {
+                    float s[M];
+#pragma unroll
+                    for (int m = 0; m < M; ++m) s[m] = v[m];
+                    // unrolled to the largest cluster (loads predicated on the rank count,
+                    // so they issue back to back); the additions stay in rank order
+#pragma unroll
+                    for (int rr = 1; rr < kMaxSplit; ++rr) {
+                        if (rr < split) {
+                            const float *pr = red + ((rr - 1) * kRows + row) * RC;
+                            if constexpr (RC == 1) {
+                                s[0] += pr[0];
+                            } else if constexpr (RC == 2) {
+                                const float2 q = *reinterpret_cast<const float2 *>(pr);
+                                s[0] += q.x;
+                                s[M > 1 ? 1 : 0] += M > 1 ? q.y : 0.0f;
+                            } else {
+#pragma unroll
+                                for (int c = 0; c < RC; c += 4) {
+                                    const float4 q = *reinterpret_cast<const float4 *>(pr + c);
+                                    const float qv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j)
+                                        if (c + j < M) s[min(c + j, M - 1)] += qv[j];
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int m = 0; m < M; ++m) store_out(o, m, n, got ? s[m] : __int_as_float(0x7fc00000));
                 }
             }
         }
@@ -444,6 +532,15 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0 && abort_flag && bp.err) atomicOr(bp.err, 1);
+    if (split > 1 && abort_flag) {
+        // A CTA that gave up a wait may have got here before the other ranks issued their
+        // stores into rank 0.  This cluster barrier waits for every thread of the cluster
+        // that has not exited (ranks that finished normally have exited, stores issued);
+        // then rank 0 waits, bounded, for those stores to land before its shared memory goes.
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        if (rank == 0 && warp == 2 && lane == 0) (void)bar_wait_cluster(redb, 0);
+    }
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
