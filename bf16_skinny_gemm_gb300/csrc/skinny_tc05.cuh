@@ -234,6 +234,46 @@ __device__ __forceinline__ void st_async4(uint32_t dst, float a, float b, float 
         : "memory");
 }
 
+// A row's M partial sums, stored with the widest st.async its alignment allows
+// (rows of M floats: 16-byte aligned when M % 4 == 0, 8-byte when M is even).
+template <int M>
+__device__ __forceinline__ void push_partial(uint32_t dst, const float (&v)[M], uint32_t bar) {
+    if constexpr (M % 4 == 0) {
+#pragma unroll
+        for (int c = 0; c < M; c += 4) st_async4(dst + 4 * c, v[c], v[c + 1], v[c + 2], v[c + 3], bar);
+    } else if constexpr (M % 2 == 0) {
+#pragma unroll
+        for (int c = 0; c < M; c += 2) st_async2(dst + 4 * c, v[c], v[c + 1], bar);
+    } else {
+#pragma unroll
+        for (int c = 0; c < M; ++c) st_async1(dst + 4 * c, v[c], bar);
+    }
+}
+// s[m] += row[m], reading the row the same way.
+template <int M>
+__device__ __forceinline__ void add_partial(const float *row, float (&s)[M]) {
+    if constexpr (M % 4 == 0) {
+#pragma unroll
+        for (int c = 0; c < M; c += 4) {
+            const float4 q = *reinterpret_cast<const float4 *>(row + c);
+            s[c] += q.x;
+            s[c + 1] += q.y;
+            s[c + 2] += q.z;
+            s[c + 3] += q.w;
+        }
+    } else if constexpr (M % 2 == 0) {
+#pragma unroll
+        for (int c = 0; c < M; c += 2) {
+            const float2 q = *reinterpret_cast<const float2 *>(row + c);
+            s[c] += q.x;
+            s[c + 1] += q.y;
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < M; ++c) s[c] += row[c];
+    }
+}
+
 __device__ __forceinline__ int read_flag(const int *f) {
     return *reinterpret_cast<const volatile int *>(f);
 }
@@ -252,8 +292,7 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
     const int S = p.ring;
     const int NB = p.nb;
     const int stage_bytes = NB * kBoxBytes;
-    constexpr int RC = red_cols(M);
-    float *red = reinterpret_cast<float *>(ring + S * stage_bytes);  // [split-1][128][RC]
+    float *red = reinterpret_cast<float *>(ring + S * stage_bytes);  // [split-1][128][M]
 
     const Params &bp = p.base;
     const int bi = blockIdx.y;  // problem of a batched call
@@ -469,22 +508,11 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
         if (warp >= 2 && ntile > 0) {
             const int row = (warp & 3) * 32 + lane;
             if (rank > 0) {
-                const uint32_t dst = cluster_addr(saddr(red + ((rank - 1) * kRows + row) * RC), 0u);
-                const uint32_t bar = cluster_addr(redb, 0u);
-                if constexpr (RC == 1) {
-                    st_async1(dst, v[0], bar);
-                } else if constexpr (RC == 2) {
-                    st_async2(dst, v[0], v[M > 1 ? 1 : 0], bar);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < RC; c += 4)
-                        st_async4(dst + 4 * c, v[c], c + 1 < M ? v[min(c + 1, M - 1)] : 0.0f,
-                                  c + 2 < M ? v[min(c + 2, M - 1)] : 0.0f,
-                                  c + 3 < M ? v[min(c + 3, M - 1)] : 0.0f, bar);
-                }
+                push_partial<M>(cluster_addr(saddr(red + ((rank - 1) * kRows + row) * M), 0u), v,
+                                cluster_addr(redb, 0u));
             } else {
                 if (warp == 2 && lane == 0)
-                    bar_expect_tx(redb, static_cast<unsigned>((split - 1) * kRows * RC * sizeof(float)));
+                    bar_expect_tx(redb, static_cast<unsigned>((split - 1) * kRows * M * sizeof(float)));
                 const bool got = bar_wait_cluster(redb, 0);
                 if (!got) atomicExch(&abort_flag, 1);
                 const int n = t_begin * kRows + row;
@@ -495,27 +523,8 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
                     // unrolled to the largest cluster (loads predicated on the rank count,
                     // so they issue back to back); the additions stay in rank order
 #pragma unroll
-                    for (int rr = 1; rr < kMaxSplit; ++rr) {
-                        if (rr < split) {
-                            const float *pr = red + ((rr - 1) * kRows + row) * RC;
-                            if constexpr (RC == 1) {
-                                s[0] += pr[0];
-                            } else if constexpr (RC == 2) {
-                                const float2 q = *reinterpret_cast<const float2 *>(pr);
-                                s[0] += q.x;
-                                s[M > 1 ? 1 : 0] += M > 1 ? q.y : 0.0f;
-                            } else {
-#pragma unroll
-                                for (int c = 0; c < RC; c += 4) {
-                                    const float4 q = *reinterpret_cast<const float4 *>(pr + c);
-                                    const float qv[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                                    for (int j = 0; j < 4; ++j)
-                                        if (c + j < M) s[min(c + j, M - 1)] += qv[j];
-                                }
-                            }
-                        }
-                    }
+                    for (int rr = 1; rr < kMaxSplit; ++rr)
+                        if (rr < split) add_partial<M>(red + ((rr - 1) * kRows + row) * M, s);
 #pragma unroll
                     for (int m = 0; m < M; ++m) store_out(o, m, n, got ? s[m] : __int_as_float(0x7fc00000));
                 }

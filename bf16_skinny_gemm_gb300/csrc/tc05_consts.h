@@ -17,12 +17,5 @@ constexpr int kMaxRingSlots = 16;               // shared-memory stages
 constexpr int kMaxNb = 4;                       // boxes per stage
 constexpr int kMaxSplit = 16;                   // CTAs of a cluster sharing a tile
 
-// Floats per row of a rank's partial tile in rank 0's reduction buffer: M
-// rounded up to a whole 8- or 16-byte store.
-#if defined(__CUDACC__)
-__host__ __device__
-#endif
-constexpr int red_cols(int M) { return M <= 2 ? M : (M + 3) / 4 * 4; }
-
 }  // namespace tc05
 }  // namespace sk

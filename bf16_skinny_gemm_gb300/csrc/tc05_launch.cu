@@ -75,7 +75,7 @@ int tc05_splits_used(int K, int split) {
 size_t tc05_smem_bytes(int M, int ring, int nb, int splits_used) {
     // the ring, the cluster-reduction buffer of rank 0, and 1 KiB of alignment slack
     return static_cast<size_t>(ring) * nb * tc05::kBoxBytes +
-           static_cast<size_t>(splits_used - 1) * tc05::red_cols(M) * tc05::kRows * sizeof(float) + 1024;
+           static_cast<size_t>(splits_used - 1) * M * tc05::kRows * sizeof(float) + 1024;
 }
 
 cudaError_t tc05_launch(const Params &base, int batch, int M, const sgemm_plan_t &plan,
