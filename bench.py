@@ -37,6 +37,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -167,32 +168,52 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
+    PERIOD_MS = 20
+
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.first = 0
+        self.reader = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln)
 
     def start(self):
+        """Start sampling and return once the first sample is in (at most 2 s), so that
+        the timed region that follows is sampled from its beginning; samples taken
+        before this returns are not counted."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        t0 = time.monotonic()
+        while not self.lines and time.monotonic() - t0 < 2.0 and self.proc.poll() is None:
+            time.sleep(0.005)
+        self.first = len(self.lines)
 
     def stop(self):
         if self.proc is None:
             return None
+        n_in_region = len(self.lines)
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+            self.proc.wait()
+        self.reader.join(timeout=5)
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in out.splitlines():
+        for ln in self.lines[self.first:n_in_region]:
             p = [v.strip() for v in ln.split(",")]
             if len(p) < 9:
                 continue

@@ -85,3 +85,41 @@ def test_algorithmic_bytes(M, N, K, expect):
     sys.path.insert(0, ROOT)
     import bench
     assert bench.gemm_bytes(M, N, K) == expect
+
+
+def test_clock_sampler_counts_only_the_timed_region(tmp_path, monkeypatch):
+    """The bench's nvidia-smi sampler, against a fake nvidia-smi on PATH: samples
+    before start() returns are not counted, throttle reasons are collected."""
+    import time
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text(
+        "#!/bin/bash\n"
+        "echo '0, 1000, 2070, 100.0, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+        "while true; do\n"
+        "  echo '0, 2070, 2070, 900.5, 0x4, Not Active, Not Active, Not Active, Active'\n"
+        "  sleep 0.02\n"
+        "done\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}:{os.environ['PATH']}")
+    s = bench.ClockSampler(0)
+    s.start()
+    time.sleep(0.2)
+    c = s.stop()
+    assert c is not None and c["samples"] >= 3
+    assert c["sm_mhz"] == 2070.0  # the 1000 MHz line came before start() returned
+    assert c["sm_max_mhz"] == 2070.0
+    assert c["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    monkeypatch.setenv("PATH", str(tmp_path))
+    s = bench.ClockSampler(0)
+    s.start()
+    assert s.stop() is None

@@ -85,8 +85,10 @@ def test_ragged_shapes(M, N, K):
 
 # ------------------------------------------------------------ plan geometry
 @pytest.mark.parametrize("split", [1, 2, 3, 5, 8, 16])
-@pytest.mark.parametrize("M", [1, 4, 8])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_cluster_splits(M, split):
+    """Every M: the other ranks push rows of M partial sums with 16-byte (M = 4, 8),
+    8-byte (M = 2, 6) or 4-byte (odd M) stores into rank 0."""
     N, K = 613, 2600  # 41 boxes of K: ragged last box, splits of 21/14/9/6/3 boxes
     x, W = _inputs(M, N, K, seed=20 + split)
     y = _run(x, W, tc05(split=split))
