@@ -213,65 +213,12 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) 
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
     return remote;
 }
-// Asynchronous stores of 1, 2 or 4 words into another CTA's shared memory
-// (shared::cluster addresses); each completes its bytes on mbarrier `bar` there.
+// Asynchronous store of one word into another CTA's shared memory (shared::cluster
+// addresses); it completes its 4 bytes on mbarrier `bar` there.
 __device__ __forceinline__ void st_async1(uint32_t dst, float a, uint32_t bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst),
                  "r"(__float_as_uint(a)), "r"(bar)
                  : "memory");
-}
-__device__ __forceinline__ void st_async2(uint32_t dst, float a, float b, uint32_t bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(
-                     dst),
-                 "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(bar)
-                 : "memory");
-}
-__device__ __forceinline__ void st_async4(uint32_t dst, float a, float b, float c, float d, uint32_t bar) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
-        "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)), "r"(__float_as_uint(d)),
-        "r"(bar)
-        : "memory");
-}
-
-// A row's M partial sums, stored with the widest st.async its alignment allows
-// (rows of M floats: 16-byte aligned when M % 4 == 0, 8-byte when M is even).
-template <int M>
-__device__ __forceinline__ void push_partial(uint32_t dst, const float (&v)[M], uint32_t bar) {
-    if constexpr (M % 4 == 0) {
-#pragma unroll
-        for (int c = 0; c < M; c += 4) st_async4(dst + 4 * c, v[c], v[c + 1], v[c + 2], v[c + 3], bar);
-    } else if constexpr (M % 2 == 0) {
-#pragma unroll
-        for (int c = 0; c < M; c += 2) st_async2(dst + 4 * c, v[c], v[c + 1], bar);
-    } else {
-#pragma unroll
-        for (int c = 0; c < M; ++c) st_async1(dst + 4 * c, v[c], bar);
-    }
-}
-// s[m] += row[m], reading the row the same way.
-template <int M>
-__device__ __forceinline__ void add_partial(const float *row, float (&s)[M]) {
-    if constexpr (M % 4 == 0) {
-#pragma unroll
-        for (int c = 0; c < M; c += 4) {
-            const float4 q = *reinterpret_cast<const float4 *>(row + c);
-            s[c] += q.x;
-            s[c + 1] += q.y;
-            s[c + 2] += q.z;
-            s[c + 3] += q.w;
-        }
-    } else if constexpr (M % 2 == 0) {
-#pragma unroll
-        for (int c = 0; c < M; c += 2) {
-            const float2 q = *reinterpret_cast<const float2 *>(row + c);
-            s[c] += q.x;
-            s[c + 1] += q.y;
-        }
-    } else {
-#pragma unroll
-        for (int c = 0; c < M; ++c) s[c] += row[c];
-    }
 }
 
 __device__ __forceinline__ int read_flag(const int *f) {
@@ -292,7 +239,7 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
     const int S = p.ring;
     const int NB = p.nb;
     const int stage_bytes = NB * kBoxBytes;
-    float *red = reinterpret_cast<float *>(ring + S * stage_bytes);  // [split-1][128][M]
+    float *red = reinterpret_cast<float *>(ring + S * stage_bytes);  // [split-1][M][128]
 
     const Params &bp = p.base;
     const int bi = blockIdx.y;  // problem of a batched call
@@ -508,8 +455,11 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
         if (warp >= 2 && ntile > 0) {
             const int row = (warp & 3) * 32 + lane;
             if (rank > 0) {
-                push_partial<M>(cluster_addr(saddr(red + ((rank - 1) * kRows + row) * M), 0u), v,
-                                cluster_addr(redb, 0u));
+                // [rank-1][m][row]: each store of a warp is 128 contiguous bytes
+                const uint32_t dst = cluster_addr(saddr(red + (rank - 1) * M * kRows + row), 0u);
+                const uint32_t bar = cluster_addr(redb, 0u);
+#pragma unroll
+                for (int m = 0; m < M; ++m) st_async1(dst + 4u * static_cast<uint32_t>(m * kRows), v[m], bar);
             } else {
                 if (warp == 2 && lane == 0)
                     bar_expect_tx(redb, static_cast<unsigned>((split - 1) * kRows * M * sizeof(float)));
@@ -523,8 +473,12 @@ __global__ void __launch_bounds__(kThreads) skinny_tc05_kernel(const __grid_cons
                     // unrolled to the largest cluster (loads predicated on the rank count,
                     // so they issue back to back); the additions stay in rank order
 #pragma unroll
-                    for (int rr = 1; rr < kMaxSplit; ++rr)
-                        if (rr < split) add_partial<M>(red + ((rr - 1) * kRows + row) * M, s);
+                    for (int rr = 1; rr < kMaxSplit; ++rr) {
+                        if (rr < split) {
+#pragma unroll
+                            for (int m = 0; m < M; ++m) s[m] += red[((rr - 1) * M + m) * kRows + row];
+                        }
+                    }
 #pragma unroll
                     for (int m = 0; m < M; ++m) store_out(o, m, n, got ? s[m] : __int_as_float(0x7fc00000));
                 }
