@@ -64,9 +64,8 @@ def gemm_bytes(M, N, K):
 def launches_per_gemm(sk, plan):
     """Kernel launches of one GEMM: split-K plans of the streaming and 16-row
     tensor-core kernels add a second-pass reduce; the tcgen05 kernel reduces
-    its K split inside a cluster and the warp-owned-tile kernel inside a CTA."""
-    one_launch = (sk.SGEMM_VARIANT_TC05, sk.SGEMM_VARIANT_MMA_TW)
-    return 2 if plan.split_k > 1 and plan.variant not in one_launch else 1
+    its K split inside a cluster."""
+    return 2 if plan.split_k > 1 and plan.variant != sk.SGEMM_VARIANT_TC05 else 1
 
 
 # --------------------------------------------------------------------- helpers
@@ -126,8 +125,7 @@ def measured_peaks():
 
 # The streaming kernels' sources, their compiled configurations, the plan table and
 # the launch geometry: what the recorded DRAM traffic per launch depends on.
-KERNEL_SOURCES = ["skinny_ldg.cuh", "skinny_mma.cuh", "skinny_mmat.cuh", "skinny_mmatw.cuh",
-                  "skinny_tc05.cuh", "tc05_consts.h", "tc05_launch.cu",
+KERNEL_SOURCES = ["skinny_ldg.cuh", "skinny_mma.cuh", "skinny_tc05.cuh", "tc05_consts.h", "tc05_launch.cu",
                   "kernel_table.cuh", "internal.h", "plan_table.inc", "api.cpp"]
 
 

@@ -28,8 +28,8 @@ __all__ = [
     "sgemm_bf16_skinny_rescale_ex", "sgemm_bf16_skinny_f32out_ex",
     "SGEMM_OK", "SGEMM_ERR_INVALID_ARG", "SGEMM_ERR_UNSUPPORTED_SHAPE", "SGEMM_ERR_MISALIGNED",
     "SGEMM_ERR_UNSUPPORTED_DEVICE", "SGEMM_ERR_NO_WORKSPACE", "SGEMM_ERR_CUDA", "MAX_BATCH",
-    "SGEMM_VARIANT_LDG", "SGEMM_VARIANT_LDG_MIXFMA", "SGEMM_VARIANT_MMA", "SGEMM_VARIANT_MMA_T", "SGEMM_VARIANT_LDG_FFMA2", "SGEMM_VARIANT_LDGX_MIXFMA",
-    "SGEMM_VARIANT_LDGX_FFMA2", "SGEMM_VARIANT_MMA_TW", "SGEMM_VARIANT_LDG_MMA",
+    "SGEMM_VARIANT_LDG", "SGEMM_VARIANT_LDG_MIXFMA", "SGEMM_VARIANT_MMA", "SGEMM_VARIANT_LDG_FFMA2",
+    "SGEMM_VARIANT_LDGX_MIXFMA", "SGEMM_VARIANT_LDGX_FFMA2", "SGEMM_VARIANT_LDG_MMA",
     "SGEMM_VARIANT_TC05", "SGEMM_FLAG_PDL",
     "SGEMM_FLAG_TEST_STALL", "sgemm_device_errors",
     "SGEMM_FLAG_WEIGHTS_READONLY",
@@ -46,11 +46,9 @@ MAX_BATCH = 8
 SGEMM_VARIANT_LDG = 0
 SGEMM_VARIANT_LDG_MIXFMA = 1
 SGEMM_VARIANT_MMA = 2
-SGEMM_VARIANT_MMA_T = 3
 SGEMM_VARIANT_LDG_FFMA2 = 5
 SGEMM_VARIANT_LDGX_MIXFMA = 6
 SGEMM_VARIANT_LDGX_FFMA2 = 7
-SGEMM_VARIANT_MMA_TW = 8
 SGEMM_VARIANT_LDG_MMA = 9
 SGEMM_VARIANT_TC05 = 10
 SGEMM_FLAG_TEST_STALL = 4

@@ -110,8 +110,7 @@ sgemm_status_t check_plan(const sgemm_plan_t &p, int M, int N, int K) {
     if (p.variant == SGEMM_VARIANT_TC05) return check_tc05_plan(p, M, K);
     if (p.variant != SGEMM_VARIANT_LDG && p.variant != SGEMM_VARIANT_LDG_MIXFMA &&
         p.variant != SGEMM_VARIANT_LDG_FFMA2 && p.variant != SGEMM_VARIANT_MMA &&
-        p.variant != SGEMM_VARIANT_MMA_T && p.variant != SGEMM_VARIANT_LDGX_MIXFMA &&
-        p.variant != SGEMM_VARIANT_LDGX_FFMA2 && p.variant != SGEMM_VARIANT_MMA_TW &&
+        p.variant != SGEMM_VARIANT_LDGX_MIXFMA && p.variant != SGEMM_VARIANT_LDGX_FFMA2 &&
         p.variant != SGEMM_VARIANT_LDG_MMA)
         return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.threads < 32 || p.threads > sk::kMaxThreads || p.threads % 32) return SGEMM_ERR_UNSUPPORTED_SHAPE;
@@ -120,16 +119,8 @@ sgemm_status_t check_plan(const sgemm_plan_t &p, int M, int N, int K) {
     if (p.ctas_per_sm < 0 || p.ctas_per_sm > 32) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (!find_kernel(p.variant, M, p.rows_per_warp, p.lanes_per_row, p.k_unroll, p.stages))
         return SGEMM_ERR_UNSUPPORTED_SHAPE;
-    if ((p.variant == SGEMM_VARIANT_MMA || p.variant == SGEMM_VARIANT_MMA_T) && p.threads < 64)
+    if (p.variant == SGEMM_VARIANT_MMA && p.threads < 64)
         return SGEMM_ERR_UNSUPPORTED_SHAPE;
-    if (p.variant == SGEMM_VARIANT_MMA_TW) {
-        // split_k = warps sharing a tile's K range inside the CTA
-        const int ks = p.split_k, nw = p.threads / 32;
-        if ((ks != 1 && ks != 2 && ks != 4 && ks != 8) || nw % ks) return SGEMM_ERR_UNSUPPORTED_SHAPE;
-        if (ks > (K / 8 + 3) / 4) return SGEMM_ERR_UNSUPPORTED_SHAPE;  // a k-block per warp at least
-        if (sk::smem_bytes(p, M, K) > kMaxSmem) return SGEMM_ERR_UNSUPPORTED_SHAPE;
-        return SGEMM_OK;
-    }
     const int kps = sk::split_kps(K, p.split_k);
     if (static_cast<long long>(p.split_k - 1) * kps >= K) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (sk::smem_bytes(p, M, kps) > kMaxSmem) return SGEMM_ERR_UNSUPPORTED_SHAPE;
@@ -390,9 +381,8 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
                                        plan.k_unroll, plan.stages);
     if (plan.variant == SGEMM_VARIANT_TC05) return run_tc05(items, batch, M, N, K, plan, flags,
                                                             stream, ep, *st, ki->fn);
-    const bool tw = plan.variant == SGEMM_VARIANT_MMA_TW;  // split_k splits K inside a CTA
-    const int split = tw ? 1 : plan.split_k;
-    const int kps = tw ? K : sk::split_kps(K, split);
+    const int split = plan.split_k;
+    const int kps = sk::split_kps(K, split);
     const size_t smem = sk::smem_bytes(plan, M, kps);
 
     sk::Params prm;
@@ -412,7 +402,7 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
     prm.N = N;
     prm.K = K;
     prm.kps = kps;
-    prm.split = tw ? plan.split_k : split;
+    prm.split = split;
     prm.row_groups = sk::work_units(plan, N);
     prm.flags = static_cast<int>(flags);
 
@@ -495,24 +485,12 @@ size_t smem_bytes(const sgemm_plan_t &plan, int M, int kps) {
         return static_cast<size_t>(M) * (chunks + 1) * 16 +
                2 * static_cast<size_t>(plan.threads / 32) * 16 * (M <= 4 ? 4 : 8) * sizeof(float);
     }
-    if (plan.variant == SGEMM_VARIANT_MMA_TW) {
-        // x rows padded by one chunk, plus two buffers of [NW][32 lanes][2] partial fragments
-        return static_cast<size_t>(M) * (chunks + 1) * 16 +
-               2 * static_cast<size_t>(plan.threads / 32) * 32 * 2 * sizeof(float);
-    }
-    if (plan.variant == SGEMM_VARIANT_MMA_T) {
-        // x rows padded by one chunk, plus two reduction buffers [NW][8][M] floats
-        return static_cast<size_t>(M) * (chunks + 1) * 16 +
-               2 * static_cast<size_t>(plan.threads / 32) * 8 * M * sizeof(float);
-    }
     return static_cast<size_t>(M) * chunks * 16;
 }
 
 int work_units(const sgemm_plan_t &plan, int N) {
     if (plan.variant == SGEMM_VARIANT_TC05) return (N + tc05::kRows - 1) / tc05::kRows;
     if (plan.variant == SGEMM_VARIANT_MMA) return (N + 15) / 16;
-    if (plan.variant == SGEMM_VARIANT_MMA_T || plan.variant == SGEMM_VARIANT_MMA_TW)
-        return (N + 7) / 8;
     const int rows_per_task = (32 / plan.lanes_per_row) * plan.rows_per_warp;
     return (N + rows_per_task - 1) / rows_per_task;
 }
@@ -527,13 +505,8 @@ cudaError_t allow_max_dynamic_smem(const void *fn) {
 
 long long ctas_wanted(const sgemm_plan_t &plan, int N) {
     const long long units = work_units(plan, N);
-    if (plan.variant == SGEMM_VARIANT_MMA || plan.variant == SGEMM_VARIANT_MMA_T ||
-        plan.variant == SGEMM_VARIANT_TC05)
+    if (plan.variant == SGEMM_VARIANT_MMA || plan.variant == SGEMM_VARIANT_TC05)
         return units;  // one tile per CTA at most
-    if (plan.variant == SGEMM_VARIANT_MMA_TW) {
-        const int groups = std::max(1, plan.threads / 32 / std::max(1, plan.split_k));
-        return (units + groups - 1) / groups;  // one tile per warp group at most
-    }
     const int warps = plan.threads / 32;
     return (units + warps - 1) / warps;
 }

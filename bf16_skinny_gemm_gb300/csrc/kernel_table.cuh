@@ -9,8 +9,6 @@
 
 #include "skinny_ldg.cuh"
 #include "skinny_mma.cuh"
-#include "skinny_mmat.cuh"
-#include "skinny_mmatw.cuh"
 #include "skinny_tc05.cuh"
 
 #define SK_LDG_CONFIGS(X, M)   \
@@ -80,34 +78,6 @@
     {SGEMM_VARIANT_MMA, M, 16, 4, U, (DB) ? 2 : 1,      \
      reinterpret_cast<const void *>(&skinny_mma_kernel<M, U, DB>)},
 
-// Tensor-core kernel with x as the A operand and warp-owned 8-row tiles:
-// (M, k-blocks per batch U, double-buffered).  R = 8, LPR = 4.
-#define SK_MMATW_CONFIGS(X, M) \
-    X(M, 4, false)             \
-    X(M, 8, false)             \
-    X(M, 16, false)            \
-    X(M, 2, true)              \
-    X(M, 4, true)              \
-    X(M, 8, true)
-
-#define SK_MMATW_ENTRY(M, U, DB)                         \
-    {SGEMM_VARIANT_MMA_TW, M, 8, 4, U, (DB) ? 2 : 1,     \
-     reinterpret_cast<const void *>(&skinny_mmatw_kernel<M, U, DB>)},
-
-// Tensor-core configurations with x as the A operand: (M, U, double-buffered).
-// R = 8 rows per tile, 4 lanes share a row segment.
-#define SK_MMAT_CONFIGS(X, M) \
-    X(M, 2, false)            \
-    X(M, 4, false)            \
-    X(M, 8, false)            \
-    X(M, 2, true)             \
-    X(M, 4, true)             \
-    X(M, 8, true)
-
-#define SK_MMAT_ENTRY(M, U, DB)                            \
-    {SGEMM_VARIANT_MMA_T, M, 8, 4, U, (DB) ? 2 : 1,        \
-     reinterpret_cast<const void *>(&skinny_mmat_kernel<M, U, DB>)},
-
 // TMA + tcgen05 kernel: one instantiation per M; tile rows 128, and the ring
 // depth, boxes per stage and cluster split are launch parameters (U = 0,
 // stages = 0 mark "any").
@@ -116,7 +86,4 @@
 
 #define SK_DEFINE_TABLE(M, NAME)                                                          \
     const KernelInfo NAME[] = {SK_LDG_CONFIGS(SK_LDG_ENTRY, M) SK_MMA_CONFIGS(SK_MMA_ENTRY, M) \
-                                   SK_MMAT_CONFIGS(SK_MMAT_ENTRY, M)     \
-                                       SK_LDGX_CONFIGS(SK_LDGX_ENTRY, M)   \
-                                           SK_MMATW_CONFIGS(SK_MMATW_ENTRY, M) \
-                                               SK_TC05_ENTRY(M)};
+                                   SK_LDGX_CONFIGS(SK_LDGX_ENTRY, M) SK_TC05_ENTRY(M)};

@@ -133,12 +133,6 @@ extern "C" sgemm_status_t sgemm_splitk_noalloc_plan(int N, int K, int M, int spl
         // the tcgen05 kernel reduces its split inside a cluster, without scratch: the
         // CUDA-core streaming kernel with split_k splits
         plan = streaming_plan(split_k);
-    } else if (plan.variant == SGEMM_VARIANT_MMA_TW) {
-        // its split_k splits K inside a CTA: the x-as-A kernel with CTA-wide tiles and
-        // the same math, at most 8 k-blocks per batch (the unrolls that kernel has)
-        plan.variant = SGEMM_VARIANT_MMA_T;
-        if (plan.k_unroll > 8) plan.k_unroll = 8;
-        plan.ctas_per_sm = 0;
     }
     *out = plan;
     return sgemm_plan_check(out, M, N, K);

@@ -51,9 +51,6 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 DEFAULT_OUT = os.path.join(HERE, "csrc", "plan_table.inc")
 
 
-# warp-owned-tile tensor-core kernel: warps sharing a tile's K range x CTAs per SM
-TW_SPLITS = [1, 2, 4, 8]
-TW_CTAS = [0, 1, 2]
 # TMA + tcgen05 kernel: (ring slots, 64-element boxes per stage), cluster splits of K,
 # and CTAs per SM of the persistent grid (split 1 only)
 TC05_GEOMETRY = [(4, 1), (6, 1), (8, 1), (12, 1), (2, 2), (3, 2), (4, 2), (6, 2), (2, 4), (3, 4)]
@@ -67,9 +64,7 @@ def candidates(M, N, K, splits, ctas=(0,)):
     out = []
     for i in range(sk.sgemm_plan_count()):
         base = sk.sgemm_plan_get(i)
-        if base.variant == sk.SGEMM_VARIANT_MMA_TW:
-            variants = [base.copy(split_k=s, ctas_per_sm=c) for s in TW_SPLITS for c in TW_CTAS]
-        elif base.variant == sk.SGEMM_VARIANT_TC05:
+        if base.variant == sk.SGEMM_VARIANT_TC05:
             if base.k_unroll != 1:
                 continue  # the enumeration lists this kernel twice; its geometry is swept here
             variants = [base.copy(stages=r, k_unroll=nb, split_k=s, ctas_per_sm=c)

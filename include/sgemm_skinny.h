@@ -82,9 +82,7 @@ typedef struct {
     int lanes_per_row;    /* lanes sharing one row: 32, 16 or 8 (16/8 suit small K) */
     int k_unroll;         /* 16-byte W loads per row per lane kept in flight */
     int vec_bytes;        /* bytes per W load: 16 */
-    int split_k;          /* K split across this many CTAs (1 = none); for
-                             SGEMM_VARIANT_MMA_TW, the warps of one CTA sharing each
-                             tile's K range (1, 2, 4 or 8), with no second pass */
+    int split_k;          /* K split across this many CTAs (1 = none) */
     int stages;           /* pipeline depth: batches of loads in flight per warp, 1 or 2
                              (2 = double-buffered batches; 0 is read as 1) */
     int ctas_per_sm;      /* resident CTAs per SM the grid is sized for (0 = occupancy max) */
@@ -102,10 +100,9 @@ enum {
                                      each 16-row tile's K range and adds the NW partial tiles in
                                      shared memory.  rows_per_warp = 16, lanes_per_row = 4,
                                      k_unroll = 32-element k-blocks per batch */
-    SGEMM_VARIANT_MMA_T = 3,      /* tensor cores with x as the A operand (rows m < M) and 8 rows
-                                     of W as the B operand: 8-row tiles, each lane streams 16 B of
-                                     one row per step.  rows_per_warp = 8, lanes_per_row = 4,
-                                     k_unroll = k-blocks per batch, stages = 1 or 2 batches */
+    /* 3: retired (x as the A operand of mma.sync with CTA-wide 8-row tiles; after the
+       tcgen05 kernel arrived it won no cell of the sweep); plans with variant 3 are
+       refused with SGEMM_ERR_UNSUPPORTED_SHAPE */
     /* 4: retired (a bulk-copy kernel that no sweep ever selected); plans with
        variant 4 are refused with SGEMM_ERR_UNSUPPORTED_SHAPE */
     SGEMM_VARIANT_LDG_FFMA2 = 5,  /* the streaming kernel of variant 0 with packed FP32x2 FMA
@@ -115,15 +112,8 @@ enum {
                                      use instead of staging it in shared memory (no CTA barrier
                                      before the first FMA); same results as variants 0/1 */
     SGEMM_VARIANT_LDGX_FFMA2 = 7, /* variant 5 with x read the same way; same results as 5 */
-    SGEMM_VARIANT_MMA_TW = 8,     /* the tensor-core math of variant 3 (x as A, 8-row tiles)
-                                     with warp-owned tiles: each warp streams its tiles' rows
-                                     along K on its own, with no CTA barrier after x is staged,
-                                     and writes y from its MMA fragment.  split_k here is the
-                                     number of warps of a CTA that share each tile's K range (1,
-                                     2, 4 or 8, dividing threads/32 and at most the 32-element
-                                     k-blocks of a row); they add their fragments in shared
-                                     memory, in order, with no second pass and no scratch.
-                                     rows_per_warp = 8, lanes_per_row = 4 */
+    /* 8: retired (the math of variant 3 with warp-owned tiles; it won no cell of the
+       sweep); plans with variant 8 are refused with SGEMM_ERR_UNSUPPORTED_SHAPE */
     SGEMM_VARIANT_LDG_MMA = 9,    /* the streaming kernel of variant 1 (one row's 512 bytes per
                                      load instruction, lanes_per_row = 32) with the products
                                      done by mma.sync m16n8k16: the 8 columns of B are the 8
@@ -320,9 +310,7 @@ sgemm_status_t sgemm_bf16_skinny_splitk_noalloc(const sgemm_bf16_t *x, long long
  * that way are replaced: a TMA + tcgen05 plan (SGEMM_VARIANT_TC05, whose split
  * reduces inside a cluster) by the CUDA-core streaming plan (variant
  * SGEMM_VARIANT_LDG_MIXFMA, 256 threads, 1 row per warp, 32 lanes per row,
- * k_unroll 8, 1 stage); a warp-owned-tile plan (SGEMM_VARIANT_MMA_TW) by the
- * x-as-A plan with CTA-wide tiles (SGEMM_VARIANT_MMA_T) with the same stages
- * and k_unroll capped at 8, ctas_per_sm 0.  Pure host function.  Writes *out
+ * k_unroll 8, 1 stage).  Pure host function.  Writes *out
  * and returns sgemm_plan_check of it for (M, N, K); SGEMM_ERR_INVALID_ARG for
  * a NULL out or split_k < 2. */
 sgemm_status_t sgemm_splitk_noalloc_plan(int N, int K, int M, int split_k,

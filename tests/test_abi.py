@@ -141,7 +141,8 @@ def test_bad_plans_rejected(lib):
     good = next(p for p in (sk.sgemm_plan_get(i) for i in range(sk.sgemm_plan_count()))
                 if p.variant == sk.SGEMM_VARIANT_LDG_MIXFMA and p.k_unroll == 8)
     assert sk.sgemm_plan_check(good, 1, 4096, 4096) == sk.SGEMM_OK
-    for change in ({"variant": 7}, {"variant": -1}, {"variant": 4}, {"threads": 48}, {"threads": 512}, {"vec_bytes": 8},
+    for change in ({"variant": 7}, {"variant": -1}, {"variant": 3}, {"variant": 4}, {"variant": 8},
+                   {"threads": 48}, {"threads": 512}, {"vec_bytes": 8},
                    {"split_k": 0}, {"k_unroll": 3}, {"lanes_per_row": 4}, {"stages": 3}):
         bad = good.copy(**change)
         assert sk.sgemm_plan_check(bad, 1, 4096, 4096) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE, change
@@ -277,18 +278,10 @@ def test_noalloc_plan_substitutions(lib):
     assert st == sk.SGEMM_OK
     assert (p.variant, p.threads, p.rows_per_warp, p.lanes_per_row, p.k_unroll, p.stages,
             p.split_k) == (sk.SGEMM_VARIANT_LDG_MIXFMA, 256, 1, 32, 8, 1, 4), p
-    # warp-owned tiles -> CTA-wide x-as-A tiles, the unroll capped at 8 (U = 16 exists
-    # only in the warp-owned form)
-    tw16 = kernel(sk.SGEMM_VARIANT_MMA_TW, k_unroll=16).copy(ctas_per_sm=2)
-    st, p = sk.sgemm_splitk_noalloc_plan(4096, 4096, 4, 2, tw16)
-    assert st == sk.SGEMM_OK, p
-    assert (p.variant, p.k_unroll, p.stages, p.split_k, p.ctas_per_sm) == \
-        (sk.SGEMM_VARIANT_MMA_T, 8, tw16.stages, 2, 0), p
-    for tw in (kernel(sk.SGEMM_VARIANT_MMA_TW, k_unroll=u, stages=s)
-               for u, s in ((4, 1), (8, 1), (16, 1), (2, 2), (4, 2), (8, 2))):
-        for M in (1, 4, 8):
-            st, p = sk.sgemm_splitk_noalloc_plan(4096, 4096, M, 2, tw)
-            assert st == sk.SGEMM_OK, (tw, p)
+    # a 16-row tensor-core plan keeps its kernel
+    mma = kernel(sk.SGEMM_VARIANT_MMA)
+    st, p = sk.sgemm_splitk_noalloc_plan(4096, 4096, 4, 2, mma)
+    assert st == sk.SGEMM_OK and p.as_dict() == mma.copy(split_k=2).as_dict()
     # the selected plan by default; split_k below 2 is refused
     st, p = sk.sgemm_splitk_noalloc_plan(4096, 8192, 1, 4)
     assert st == sk.SGEMM_OK and p.split_k == 4

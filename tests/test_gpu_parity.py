@@ -91,10 +91,7 @@ def test_every_plan_every_split(M, split):
     ref = oracle.skinny_gemm(xb, Wb)
     for p in _all_plans():
         plan = p.copy(split_k=split)
-        if sk.sgemm_plan_check(plan, M, N, K) != sk.SGEMM_OK:
-            # the warp-owned-tile kernel splits K inside a CTA, 1, 2, 4 or 8 ways
-            assert p.variant == sk.SGEMM_VARIANT_MMA_TW and split in (3, 5)
-            continue
+        assert sk.sgemm_plan_check(plan, M, N, K) == sk.SGEMM_OK, plan
         y = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=plan)
         torch.cuda.synchronize()
         rep = compare(synth.bits(y), ref, xb, Wb)
@@ -348,8 +345,7 @@ def test_plans_with_same_lanes_per_row_agree_bitwise(M):
                 continue
             y = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=plan)
             torch.cuda.synchronize()
-            mma = plan.variant in (sk.SGEMM_VARIANT_MMA, sk.SGEMM_VARIANT_MMA_T,
-                                   sk.SGEMM_VARIANT_MMA_TW, sk.SGEMM_VARIANT_TC05)
+            mma = plan.variant in (sk.SGEMM_VARIANT_MMA, sk.SGEMM_VARIANT_TC05)
             # the widened and the mixed-precision FMA round identically; the packed
             # FP32x2 FMA keeps two partial sums, a different order of its own
             ffma2 = plan.variant in (sk.SGEMM_VARIANT_LDG_FFMA2, sk.SGEMM_VARIANT_LDGX_FFMA2)
@@ -404,122 +400,3 @@ def test_pdl_chain_matches_plain_launches(flags, split):
     torch.cuda.synchronize()
     for a, b in zip(ref, gout):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
-
-
-# ------------------------------------------- warp-owned-tile tensor-core plans
-def _tw_plans():
-    return [p for p in _all_plans() if p.variant == sk.SGEMM_VARIANT_MMA_TW]
-
-
-def _tw_plan(threads=256, U=8, stages=1, ks=1, ctas=0):
-    for p in _tw_plans():
-        if p.threads == threads and p.k_unroll == U and p.stages == stages:
-            return p.copy(split_k=ks, ctas_per_sm=ctas)
-    raise AssertionError("no warp-owned-tile plan with these parameters compiled")
-
-
-# (1, 8): one k-block, only ks = 1 fits; (17, 256): 8 k-blocks, ragged last
-# tile; (40, 8192) and (613, 2600): ragged tile and k-block; (4096, 8192) and
-# (12576, 4096): the full-size decode shapes, sampled rows
-@pytest.mark.parametrize("N,K", [(1, 8), (17, 256), (40, 8192), (613, 2600), (1000, 1024),
-                                 (4096, 8192), (12576, 4096)])
-@pytest.mark.parametrize("ks", [1, 2, 4, 8])
-@pytest.mark.parametrize("threads", [256, 128])
-def test_warp_owned_tiles(N, K, ks, threads):
-    M = 4
-    plan = _tw_plan(threads=threads, ks=ks)
-    if (ks > threads // 32) or ks > (K // 8 + 3) // 4:
-        assert sk.sgemm_plan_check(plan, M, N, K) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE
-        return
-    assert sk.sgemm_plan_check(plan, M, N, K) == sk.SGEMM_OK
-    x, W = _inputs(M, N, K, seed=2100 + N + K)
-    xd, Wd = x.to(DEV), W.to(DEV)
-    y = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=plan)
-    y2 = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=plan)
-    torch.cuda.synchronize()
-    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
-    if N * K <= 4096 * 4096:
-        _check(x, W, y)
-    else:
-        rows = torch.as_tensor(np.unique(np.r_[np.arange(0, N, 97), N - 1]))
-        xb = synth.bits(x)
-        Wb = synth.bits(W[rows])
-        rep = compare(synth.bits(y)[:, rows.numpy()], oracle.skinny_gemm(xb, Wb), xb, Wb)
-        assert rep["ok"], rep
-
-
-@pytest.mark.parametrize("ks", [1, 2, 4])
-def test_warp_owned_tiles_bits_depend_on_k_split_only(ks):
-    """The accumulation order is fixed by (K, split): any U, batch depth, CTA
-    size and grid give the same bits."""
-    M, N, K = 3, 2000, 3000
-    x, W = _inputs(M, N, K, seed=2200 + ks)
-    xd, Wd = x.to(DEV), W.to(DEV)
-    ref = None
-    for p in _tw_plans():
-        for ctas in (0, 1, 3):
-            plan = p.copy(split_k=ks, ctas_per_sm=ctas)
-            if sk.sgemm_plan_check(plan, M, N, K) != sk.SGEMM_OK:
-                continue
-            y = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=plan)
-            torch.cuda.synchronize()
-            if ref is None:
-                ref = (plan, y)
-                _check(x, W, y)
-            else:
-                assert torch.equal(ref[1].view(torch.int16), y.view(torch.int16)), (ref[0], plan)
-    assert ref is not None
-
-
-@pytest.mark.parametrize("batch", [2, 8])
-def test_warp_owned_tiles_batched_matches_separate_calls(batch):
-    M, N, K = 3, 200, 4096
-    plan = _tw_plan(ks=4)
-    items, refs = [], []
-    for i in range(batch):
-        x, W = _inputs(M, N, K, seed=2300 + i)
-        items.append((x.to(DEV), W.to(DEV)))
-        refs.append((x, W))
-    outs = sk.sgemm_bf16_skinny_batched_ex(items, plan=plan)
-    torch.cuda.synchronize()
-    for (xd, Wd), y, (x, W) in zip(items, outs, refs):
-        sep = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=plan)
-        torch.cuda.synchronize()
-        assert torch.equal(sep.view(torch.int16), y.view(torch.int16))
-        _check(x, W, y)
-
-
-@pytest.mark.parametrize("flags", [sk.SGEMM_FLAG_PDL,
-                                   sk.SGEMM_FLAG_PDL | sk.SGEMM_FLAG_WEIGHTS_READONLY])
-def test_warp_owned_tiles_pdl_chain_matches_plain_launches(flags):
-    M = 2
-    shapes = [(12576, 4096), (4096, 4096), (2048, 4096), (4096, 2048)]
-    Ws = [synth.normal_bf16(s, synth.W_STD, seed=2400 + i).to(DEV) for i, s in enumerate(shapes)]
-    xd = synth.normal_bf16((M, 4096), 1.0, seed=2399).to(DEV)
-
-    def chain(fl):
-        outs, x = [], xd
-        for i, W in enumerate(Ws):
-            N, K = W.shape
-            y = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
-            sk.sgemm_bf16_skinny_ex(x, W, y, plan=_tw_plan(ks=1 + i % 2), flags=fl)
-            outs.append(y)
-            x = (y[:, :Ws[i + 1].shape[1]].float() * 8.0).to(torch.bfloat16) \
-                if i + 1 < len(Ws) else None
-        return outs
-
-    ref = chain(0)
-    torch.cuda.synchronize()
-    got = chain(flags)
-    torch.cuda.synchronize()
-    for a, b in zip(ref, got):
-        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
-
-
-def test_warp_owned_tiles_reject_bad_splits():
-    for ks in (3, 5, 16):
-        assert sk.sgemm_plan_check(_tw_plan(ks=ks), 1, 4096, 4096) == \
-            sk.SGEMM_ERR_UNSUPPORTED_SHAPE
-    assert sk.sgemm_plan_check(_tw_plan(threads=128, ks=8), 1, 4096, 4096) == \
-        sk.SGEMM_ERR_UNSUPPORTED_SHAPE
-    assert sk.sgemm_plan_check(_tw_plan(ks=2), 1, 4096, 32) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE
