@@ -91,7 +91,7 @@ sgemm_status_t check_tc05_plan(const sgemm_plan_t &p, int M, int K) {
     if (p.threads != sk::tc05::kThreads || p.rows_per_warp != sk::tc05::kRows ||
         p.lanes_per_row != 0 || p.vec_bytes != 16)
         return SGEMM_ERR_UNSUPPORTED_SHAPE;
-    if (p.k_unroll != 1 && p.k_unroll != 2 && p.k_unroll != 4) return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    if (p.k_unroll < 1 || p.k_unroll > sk::tc05::kMaxNb) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.stages < 2 || p.stages > sk::tc05::kMaxRingSlots) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.ctas_per_sm < 0 || p.ctas_per_sm > 8) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     const int kbox = (K + sk::tc05::kBoxK - 1) / sk::tc05::kBoxK;

@@ -53,7 +53,7 @@ DEFAULT_OUT = os.path.join(HERE, "csrc", "plan_table.inc")
 
 # TMA + tcgen05 kernel: (ring slots, 64-element boxes per stage), cluster splits of K,
 # and CTAs per SM of the persistent grid (split 1 only)
-TC05_GEOMETRY = [(4, 1), (6, 1), (8, 1), (12, 1), (2, 2), (3, 2), (4, 2), (6, 2), (2, 4), (3, 4)]
+TC05_GEOMETRY = [(4, 1), (6, 1), (8, 1), (12, 1), (2, 2), (3, 2), (4, 2), (6, 2), (2, 3), (3, 3), (4, 3), (2, 4), (3, 4)]
 TC05_SPLITS = [1, 2, 3, 4, 6, 8, 16]
 TC05_CTAS = [0, 1, 2]
 

@@ -129,7 +129,7 @@ enum {
                                      warps read the accumulator back and write y.  No W element
                                      passes through registers.  threads = 192, rows_per_warp =
                                      128 (rows per tile), lanes_per_row = 0, k_unroll = boxes
-                                     per stage (1, 2 or 4), stages = ring slots (2..16).
+                                     per stage (1..4), stages = ring slots (2..16).
                                      split_k = 1: a persistent grid of ctas_per_sm CTAs per SM
                                      (0 = occupancy) over the tiles; split_k = 2..16: the split_k
                                      CTAs of a thread-block cluster share a tile's K range (in

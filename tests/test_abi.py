@@ -215,7 +215,7 @@ def _tc05_plan():
 
 def test_tc05_plan_checks(lib):
     """Host-side checks of the TMA + tcgen05 plans: fixed geometry (192
-    threads, 128-row tiles), 1/2/4 boxes per stage, 2..16 ring slots that fit
+    threads, 128-row tiles), 1..4 boxes per stage, 2..16 ring slots that fit
     shared memory, and a cluster split of 1..16 with at least one 64-element
     box of K per split."""
     p = _tc05_plan()
@@ -225,7 +225,7 @@ def test_tc05_plan_checks(lib):
     for split in (1, 2, 3, 5, 8, 16):
         assert sk.sgemm_plan_check(p.copy(split_k=split), 4, 613, 2600) == sk.SGEMM_OK
     for change in ({"threads": 256}, {"rows_per_warp": 64}, {"lanes_per_row": 32},
-                   {"k_unroll": 3}, {"k_unroll": 8}, {"stages": 1}, {"stages": 17},
+                   {"k_unroll": 0}, {"k_unroll": 5}, {"k_unroll": 8}, {"stages": 1}, {"stages": 17},
                    {"split_k": 0}, {"split_k": 17}, {"ctas_per_sm": -1}, {"vec_bytes": 8},
                    {"stages": 16, "k_unroll": 4}):
         bad = p.copy(**change)

@@ -96,7 +96,7 @@ def test_cluster_splits(M, split):
 
 
 @pytest.mark.parametrize("ring,nb", [(2, 1), (3, 1), (8, 1), (12, 1), (2, 2), (4, 2), (6, 2),
-                                     (2, 4), (3, 4)])
+                                     (2, 3), (4, 3), (2, 4), (3, 4)])
 def test_ring_and_boxes_per_stage_do_not_change_bits(ring, nb):
     M, N, K = 3, 1500, 3072
     x, W = _inputs(M, N, K, seed=30)
@@ -284,7 +284,7 @@ def test_graph_replay_sees_in_place_weight_refresh():
 def test_plan_checks():
     ok = tc05()
     assert sk.sgemm_plan_check(ok, 1, 4096, 4096) == sk.SGEMM_OK
-    bad = [ok.copy(threads=128), ok.copy(k_unroll=3), ok.copy(stages=1), ok.copy(stages=17),
+    bad = [ok.copy(threads=128), ok.copy(k_unroll=5), ok.copy(stages=1), ok.copy(stages=17),
            ok.copy(split_k=17), ok.copy(lanes_per_row=4), ok.copy(rows_per_warp=64),
            ok.copy(stages=16, k_unroll=4)]  # 16 x 4 boxes x 18 KiB do not fit shared memory
     for p in bad:
