@@ -8,7 +8,10 @@ tensor memory and returns, so the context stays usable.  The test-only launch
 flag SGEMM_FLAG_TEST_STALL makes the kernel's producer issue no copies at all,
 so the waits run out: nothing faults, traps or hangs.  The host reads the
 status with sgemm_device_errors().  Both work splits are covered: the
-persistent grid and the cluster split whose CTAs meet at a cluster barrier.
+persistent grid, and the cluster split, whose ranks push their partial tiles
+to rank 0 (counted on an mbarrier that rank 0 waits on, bounded) and whose
+CTAs that gave up take a second cluster barrier before they exit, so that no
+partial tile lands in shared memory that has been released.
 """
 from __future__ import annotations
 
