@@ -286,3 +286,20 @@ def test_noalloc_plan_substitutions(lib):
     st, p = sk.sgemm_splitk_noalloc_plan(4096, 8192, 1, 4)
     assert st == sk.SGEMM_OK and p.split_k == 4
     assert sk.sgemm_splitk_noalloc_plan(4096, 8192, 1, 1)[0] == sk.SGEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("N,K,M", [(4096, 8192, 1), (2048, 4096, 4), (77440, 4096, 8), (1, 8, 1)])
+def test_sweep_candidates_are_valid_plans(lib, N, K, M):
+    """Every plan the offline sweep would time passes the library's own plan
+    check, no retired variant (3, 4, 8) appears, and the tcgen05 candidates
+    cover 1..4 boxes per stage."""
+    from bf16_skinny_gemm_gb300 import sweep
+
+    cands = sweep.candidates(M, N, K, [1, 2, 4])
+    assert cands
+    for p in cands:
+        assert sk.sgemm_plan_check(p, M, N, K) == sk.SGEMM_OK, p
+        assert p.variant not in (3, 4, 8), p
+    tc = [p for p in cands if p.variant == sk.SGEMM_VARIANT_TC05]
+    assert {p.k_unroll for p in tc} == {1, 2, 3, 4}
+    assert {p.stages for p in tc} >= {2, 3, 4}
