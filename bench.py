@@ -63,9 +63,10 @@ def gemm_bytes(M, N, K):
 
 def launches_per_gemm(sk, plan):
     """Kernel launches of one GEMM: split-K plans of the streaming and 16-row
-    tensor-core kernels add a second-pass reduce; the tcgen05 kernel reduces
-    its K split inside a cluster."""
-    return 2 if plan.split_k > 1 and plan.variant != sk.SGEMM_VARIANT_TC05 else 1
+    tensor-core kernels add a second-pass reduce; the tcgen05 kernel and the
+    cluster-split streaming plans reduce their K split inside a cluster."""
+    one_launch = (sk.SGEMM_VARIANT_TC05, sk.SGEMM_VARIANT_LDG_CLUSTER)
+    return 2 if plan.split_k > 1 and plan.variant not in one_launch else 1
 
 
 # --------------------------------------------------------------------- helpers

@@ -30,6 +30,7 @@ __all__ = [
     "SGEMM_ERR_UNSUPPORTED_DEVICE", "SGEMM_ERR_NO_WORKSPACE", "SGEMM_ERR_CUDA", "MAX_BATCH",
     "SGEMM_VARIANT_LDG", "SGEMM_VARIANT_LDG_MIXFMA", "SGEMM_VARIANT_MMA", "SGEMM_VARIANT_LDG_FFMA2",
     "SGEMM_VARIANT_LDGX_MIXFMA", "SGEMM_VARIANT_LDGX_FFMA2", "SGEMM_VARIANT_LDG_MMA",
+    "SGEMM_VARIANT_LDG_CLUSTER",
     "SGEMM_VARIANT_TC05", "SGEMM_FLAG_PDL",
     "SGEMM_FLAG_TEST_STALL", "sgemm_device_errors",
     "SGEMM_FLAG_WEIGHTS_READONLY",
@@ -51,6 +52,7 @@ SGEMM_VARIANT_LDGX_MIXFMA = 6
 SGEMM_VARIANT_LDGX_FFMA2 = 7
 SGEMM_VARIANT_LDG_MMA = 9
 SGEMM_VARIANT_TC05 = 10
+SGEMM_VARIANT_LDG_CLUSTER = 11
 SGEMM_FLAG_TEST_STALL = 4
 SGEMM_FLAG_PDL = 1
 SGEMM_FLAG_WEIGHTS_READONLY = 2

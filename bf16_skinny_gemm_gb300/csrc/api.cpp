@@ -58,6 +58,8 @@ const KernelInfo *table_for_m(int M) {
 const KernelInfo *find_kernel(int variant, int M, int R, int LPR, int U, int stages) {
     const KernelInfo *t = table_for_m(M);
     if (!t) return nullptr;
+    // the cluster-split plans run the kernels of the mixed-precision streaming plans
+    if (variant == SGEMM_VARIANT_LDG_CLUSTER) variant = SGEMM_VARIANT_LDG_MIXFMA;
     if (variant == SGEMM_VARIANT_TC05) {
         // one kernel per M; the rest are launch parameters
         for (int i = 0; i < sk::kKernelCountPerM; ++i)
@@ -111,8 +113,10 @@ sgemm_status_t check_plan(const sgemm_plan_t &p, int M, int N, int K) {
     if (p.variant != SGEMM_VARIANT_LDG && p.variant != SGEMM_VARIANT_LDG_MIXFMA &&
         p.variant != SGEMM_VARIANT_LDG_FFMA2 && p.variant != SGEMM_VARIANT_MMA &&
         p.variant != SGEMM_VARIANT_LDGX_MIXFMA && p.variant != SGEMM_VARIANT_LDGX_FFMA2 &&
-        p.variant != SGEMM_VARIANT_LDG_MMA)
+        p.variant != SGEMM_VARIANT_LDG_MMA && p.variant != SGEMM_VARIANT_LDG_CLUSTER)
         return SGEMM_ERR_UNSUPPORTED_SHAPE;
+    // a cluster holds at most 8 CTAs portably
+    if (p.variant == SGEMM_VARIANT_LDG_CLUSTER && p.split_k > 8) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.threads < 32 || p.threads > sk::kMaxThreads || p.threads % 32) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.vec_bytes != 16 || p.stages < 0 || p.stages > 2) return SGEMM_ERR_UNSUPPORTED_SHAPE;
     if (p.split_k < 1 || p.split_k > 64) return SGEMM_ERR_UNSUPPORTED_SHAPE;
@@ -384,6 +388,8 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
     const int split = plan.split_k;
     const int kps = sk::split_kps(K, split);
     const size_t smem = sk::smem_bytes(plan, M, kps);
+    // the split CTAs of a row range form a cluster and reduce in rank 0's shared memory
+    const bool clv = plan.variant == SGEMM_VARIANT_LDG_CLUSTER && split > 1;
 
     sk::Params prm;
     std::memset(&prm, 0, sizeof(prm));
@@ -405,11 +411,13 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
     prm.split = split;
     prm.row_groups = sk::work_units(plan, N);
     prm.flags = static_cast<int>(flags);
+    prm.cluster = clv ? 1 : 0;
+    prm.cl_rows = clv ? sk::cluster_rows(plan) : 0;
 
     int grid_x = 0;
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        if (split > 1) {
+        if (split > 1 && !clv) {
             const size_t need = static_cast<size_t>(batch) * split * M * N * sizeof(float);
             s = ensure_workspace(*st, need, stream);
             if (s != SGEMM_OK) return s;
@@ -425,7 +433,8 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
         const long long need_ctas = sk::ctas_wanted(plan, N);
         const long long slots = std::max<long long>(
             1, static_cast<long long>(st->sms) * occ / (static_cast<long long>(split) * batch));
-        grid_x = static_cast<int>(std::max<long long>(1, std::min(need_ctas, slots)));
+        // a cluster-split grid gives each warp one task at most (the size of rank 0's buffer)
+        grid_x = static_cast<int>(std::max<long long>(1, clv ? need_ctas : std::min(need_ctas, slots)));
     }
 
     cudaLaunchConfig_t cfg;
@@ -435,17 +444,26 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
     cfg.blockDim = dim3(static_cast<unsigned>(plan.threads), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    int na = 0;
     if (flags & SGEMM_FLAG_PDL) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
     }
+    if (clv) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = static_cast<unsigned>(split);
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = na ? attr : nullptr;
+    cfg.numAttrs = static_cast<unsigned>(na);
     void *args[] = {&prm};
     if (cudaLaunchKernelExC(&cfg, ki->fn, args) != cudaSuccess) return SGEMM_ERR_CUDA;
 
-    if (split > 1) {
+    if (split > 1 && !clv) {
         const long long total = static_cast<long long>(batch) * M * N;
         int blocks = static_cast<int>(std::min<long long>((total + 255) / 256, 8LL * st->sms));
         cudaLaunchConfig_t rc;
@@ -476,6 +494,12 @@ int split_kps(int K, int split) {
     return per * 8;
 }
 
+// Rows of a CTA of a cluster-split plan, whose grid gives each warp one task (one
+// row group of R * 32 / lanes_per_row rows) at most.
+int cluster_rows(const sgemm_plan_t &plan) {
+    return plan.threads / 32 * (32 / plan.lanes_per_row) * plan.rows_per_warp;
+}
+
 size_t smem_bytes(const sgemm_plan_t &plan, int M, int kps) {
     const size_t chunks = static_cast<size_t>(kps) / 8;
     if (plan.variant == SGEMM_VARIANT_LDGX_MIXFMA || plan.variant == SGEMM_VARIANT_LDGX_FFMA2)
@@ -485,7 +509,10 @@ size_t smem_bytes(const sgemm_plan_t &plan, int M, int kps) {
         return static_cast<size_t>(M) * (chunks + 1) * 16 +
                2 * static_cast<size_t>(plan.threads / 32) * 16 * (M <= 4 ? 4 : 8) * sizeof(float);
     }
-    return static_cast<size_t>(M) * chunks * 16;
+    size_t bytes = static_cast<size_t>(M) * chunks * 16;
+    if (plan.variant == SGEMM_VARIANT_LDG_CLUSTER && plan.split_k > 1)
+        bytes += static_cast<size_t>(plan.split_k) * cluster_rows(plan) * M * sizeof(float);
+    return bytes;
 }
 
 int work_units(const sgemm_plan_t &plan, int N) {

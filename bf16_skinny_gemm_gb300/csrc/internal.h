@@ -46,6 +46,9 @@ struct Params {
     int out_f32;     // 1: y holds FP32 outputs (no BF16 rounding)
     int xn_len;      // fused chain epilogue: xn[m][k] for 0 <= k < xn_len ...
     float xn_scale;  // ... = RNE_bf16(float(y[m][k mod N]) * xn_scale)
+    int cluster;     // streaming kernel: the split CTAs of a row range form a thread-block
+                     // cluster and rank 0 adds the partial sums (no ws, no second pass)
+    int cl_rows;     // ... rows per CTA that rank 0's buffer holds per split
 };
 
 // Kernel parameters of the TMA + tcgen05 kernel (skinny_tc05.cuh): the common
@@ -93,6 +96,8 @@ extern const void *const kReduceKernels[kMaxM + 1];
 int split_kps(int K, int split);
 // Dynamic shared memory of one CTA of this plan.
 size_t smem_bytes(const sgemm_plan_t &plan, int M, int kps);
+// Rows per CTA of a cluster-split streaming plan (SGEMM_VARIANT_LDG_CLUSTER).
+int cluster_rows(const sgemm_plan_t &plan);
 // Work units of this plan (row groups for the CUDA-core kernel, 16-row tiles
 // for the tensor-core kernel) and the CTAs that can use them.
 int work_units(const sgemm_plan_t &plan, int N);

@@ -73,6 +73,81 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
+// ---------------------------------------------------------------------------
+// Shared-memory mbarriers and thread-block-cluster primitives (used by the
+// tcgen05 kernel and by the streaming kernel's cluster split).
+
+__device__ __forceinline__ uint32_t saddr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void bar_init(uint32_t b, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void bar_expect_tx(uint32_t b, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes)
+                 : "memory");
+}
+
+// Whether the phase of parity `parity` of mbarrier b has completed, with
+// cluster-scope acquire: for a barrier that other CTAs of the cluster complete
+// with st.async.
+__device__ __forceinline__ bool bar_try_cluster(uint32_t b, unsigned parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(b), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool bar_wait_cluster(uint32_t b, unsigned parity) {
+    if (bar_try_cluster(b, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!bar_try_cluster(b, parity)) {
+        if (static_cast<long long>(global_ns() - t0) > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// The shared::cluster address of CTA-local shared address `local` in the
+// cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    return remote;
+}
+
+// Asynchronous store of one word into another CTA's shared memory (shared::cluster
+// addresses); it completes its 4 bytes on mbarrier `bar` there.
+__device__ __forceinline__ void st_async1(uint32_t dst, float a, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst),
+                 "r"(__float_as_uint(a)), "r"(bar)
+                 : "memory");
+}
+
 // BF16 -> FP32 is exact: the BF16 bits are the top half of the FP32 bits.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -367,6 +442,30 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
     const int g_end = static_cast<int>(RG * (blockIdx.x + 1) / gridDim.x);
     const int g0 = g_begin + warp;
     const int ntask = g0 < g_end ? (g_end - g0 + warps - 1) / warps : 0;
+
+    // Split across a thread-block cluster (p.cluster): the p.split CTAs of this row range
+    // form a cluster, rank r having K split r.  Rank 0 keeps its own partial sums and takes
+    // the other ranks' through st.async into red [split][cl_rows][M], every byte counted on
+    // its mbarrier cl_bar; it adds them in split order once they have landed.
+    __shared__ __align__(8) uint64_t cl_bar;
+    const bool cl = p.cluster != 0 && p.split > 1;
+    const int crank = cl ? static_cast<int>(cluster_rank()) : 0;
+    const int row0 = g_begin * G * R;
+    const int rows_valid = max(0, min(p.N, g_end * G * R) - row0);
+    // after the x slice of a full split (the last split's is shorter), the same offset on
+    // every rank
+    float *red = reinterpret_cast<float *>(xs + (XG ? 0 : M * (p.kps >> 3)));
+    bool cl_waited = false;
+    if (cl) {
+        if (threadIdx.x == 0) {
+            bar_init(saddr(&cl_bar), 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            if (crank == 0)  // the only arrival: the bytes the other ranks will send
+                bar_expect_tx(saddr(&cl_bar),
+                              static_cast<unsigned>((p.split - 1) * rows_valid * M * sizeof(float)));
+        }
+        cluster_arrive_relaxed();  // this CTA has started (its mbarrier exists)
+    }
     const int jtot = (nchunk + LPR - 1) / LPR;          // iterations per task
     const int last_lanes = nchunk - (jtot - 1) * LPR;   // lanes busy in a task's last iteration
     const int total = ntask * jtot;                     // iterations of this warp
@@ -486,6 +585,18 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
                                 for (int m = 0; m < M; ++m) {
                                     if (p.split == 1) {
                                         store_out(p, it, m, n, tot[m][r]);
+                                    } else if (cl) {
+                                        const int rl = n - row0;
+                                        if (crank == 0) {
+                                            red[rl * M + m] = tot[m][r];
+                                        } else if (!(p.flags & kFlagTestStall)) {
+                                            if (!cl_waited) {
+                                                cluster_wait_acquire();  // rank 0 has started
+                                                cl_waited = true;
+                                            }
+                                            st_async1(cluster_addr(saddr(red + (crank * p.cl_rows + rl) * M + m), 0u),
+                                                      tot[m][r], cluster_addr(saddr(&cl_bar), 0u));
+                                        }
                                     } else {
                                         const long long slot =
                                             (static_cast<long long>(blockIdx.z) * p.split + s) * M + m;
@@ -521,6 +632,34 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
         for (int base = 0; base < total; base += U) {
             consume_batch(bufA, base);
             if (base + U < total) issue_batch(bufA, base + U);
+        }
+    }
+
+    if (cl) {
+        // every thread waits once on the start barrier it arrived on (long complete)
+        if (!cl_waited) cluster_wait_acquire();
+        if (crank == 0) {
+            __syncthreads();  // this CTA's own partial sums are in red
+            const bool got = bar_wait_cluster(saddr(&cl_bar), 0);
+            const bool bad = __syncthreads_or(!got) != 0;
+            for (int i = threadIdx.x; i < rows_valid * M; i += blockDim.x) {
+                const int rl = i / M;
+                const int m = i - rl * M;
+                // split order from 0.0f, as the second-pass kernel adds: the same bits
+                float acc = 0.0f;
+                for (int q = 0; q < p.split; ++q) acc += red[(q * p.cl_rows + rl) * M + m];
+                store_out(p, it, m, row0 + rl, bad ? __int_as_float(0x7fc00000) : acc);
+            }
+            if (bad) {
+                // a rank's partials did not all land in time: report it, then wait until
+                // every other rank has issued its stores (this barrier waits for the
+                // threads of the cluster that have not exited), and for those to land,
+                // before this CTA's shared memory goes
+                if (threadIdx.x == 0 && p.err) atomicOr(p.err, 1);
+                cluster_arrive_release();
+                cluster_wait_acquire();
+                if (threadIdx.x == 0) (void)bar_wait_cluster(saddr(&cl_bar), 0);
+            }
         }
     }
 }

@@ -80,35 +80,8 @@ constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                             (static_cast<uint32_t>(kCols >> 3) << 17) |
                             (static_cast<uint32_t>(kRows >> 4) << 24);
 
-__device__ __forceinline__ uint32_t saddr(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void bar_init(uint32_t b, unsigned count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b), "r"(count) : "memory");
-}
-
 __device__ __forceinline__ void bar_arrive(uint32_t b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(b) : "memory");
-}
-
-__device__ __forceinline__ void bar_expect_tx(uint32_t b, unsigned bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes)
-                 : "memory");
-}
-
-// As bar_try, with cluster-scope acquire: for a barrier that other CTAs of the
-// cluster complete with st.async.
-__device__ __forceinline__ bool bar_try_cluster(uint32_t b, unsigned parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(b), "r"(parity)
-        : "memory");
-    return ok != 0;
 }
 
 __device__ __forceinline__ bool bar_try(uint32_t b, unsigned parity) {
@@ -129,14 +102,6 @@ __device__ __forceinline__ bool bar_wait(uint32_t b, unsigned parity) {
     if (bar_try(b, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!bar_try(b, parity)) {
-        if (static_cast<long long>(global_ns() - t0) > kWaitLimitNs) return false;
-    }
-    return true;
-}
-__device__ __forceinline__ bool bar_wait_cluster(uint32_t b, unsigned parity) {
-    if (bar_try_cluster(b, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    while (!bar_try_cluster(b, parity)) {
         if (static_cast<long long>(global_ns() - t0) > kWaitLimitNs) return false;
     }
     return true;
@@ -192,34 +157,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_arrive_release() {
-    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait_acquire() {
-    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
-}
-// The shared::cluster address of CTA-local shared address `local` in the
-// cluster's CTA `rank`.
-__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
-    return remote;
-}
-// Asynchronous store of one word into another CTA's shared memory (shared::cluster
-// addresses); it completes its 4 bytes on mbarrier `bar` there.
-__device__ __forceinline__ void st_async1(uint32_t dst, float a, uint32_t bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst),
-                 "r"(__float_as_uint(a)), "r"(bar)
-                 : "memory");
-}
 
 __device__ __forceinline__ int read_flag(const int *f) {
     return *reinterpret_cast<const volatile int *>(f);

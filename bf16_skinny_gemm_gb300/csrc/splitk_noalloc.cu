@@ -133,6 +133,8 @@ extern "C" sgemm_status_t sgemm_splitk_noalloc_plan(int N, int K, int M, int spl
         // the tcgen05 kernel reduces its split inside a cluster, without scratch: the
         // CUDA-core streaming kernel with split_k splits
         plan = streaming_plan(split_k);
+    } else if (plan.variant == SGEMM_VARIANT_LDG_CLUSTER) {
+        plan.variant = SGEMM_VARIANT_LDG_MIXFMA;  // the same kernel, split through the array
     }
     *out = plan;
     return sgemm_plan_check(out, M, N, K);

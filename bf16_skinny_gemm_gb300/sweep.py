@@ -56,6 +56,8 @@ DEFAULT_OUT = os.path.join(HERE, "csrc", "plan_table.inc")
 TC05_GEOMETRY = [(4, 1), (6, 1), (8, 1), (12, 1), (2, 2), (3, 2), (4, 2), (6, 2), (2, 3), (3, 3), (4, 3), (2, 4), (3, 4)]
 TC05_SPLITS = [1, 2, 3, 4, 6, 8, 16]
 TC05_CTAS = [0, 1, 2]
+# cluster-split streaming plans: CTAs of a cluster sharing a row range's K
+LDG_CLUSTER_SPLITS = [2, 3, 4, 6, 8]
 
 
 def candidates(M, N, K, splits, ctas=(0,)):
@@ -64,7 +66,12 @@ def candidates(M, N, K, splits, ctas=(0,)):
     out = []
     for i in range(sk.sgemm_plan_count()):
         base = sk.sgemm_plan_get(i)
-        if base.variant == sk.SGEMM_VARIANT_TC05:
+        if base.variant == sk.SGEMM_VARIANT_LDG_MIXFMA:
+            # also as the cluster-split plan (one launch, no second pass)
+            variants = [base.copy(split_k=s, ctas_per_sm=c) for s in splits for c in ctas]
+            variants += [base.copy(variant=sk.SGEMM_VARIANT_LDG_CLUSTER, split_k=s)
+                         for s in LDG_CLUSTER_SPLITS]
+        elif base.variant == sk.SGEMM_VARIANT_TC05:
             if base.k_unroll != 1:
                 continue  # the enumeration lists this kernel twice; its geometry is swept here
             variants = [base.copy(stages=r, k_unroll=nb, split_k=s, ctas_per_sm=c)
@@ -257,6 +264,8 @@ def main(argv=None):
     ap.add_argument("--min-bytes", type=float, default=float(1 << 30))
     ap.add_argument("--shapes", default=None, help="e.g. 4096x4096,2048x4096 (default: all)")
     ap.add_argument("--no-pair", action="store_true")
+    ap.add_argument("--note", default="",
+                    help="appended to the table's header line (where its entries came from)")
     ap.add_argument("--merge", default=None,
                     help="start from this existing table and replace only the swept entries")
     ap.add_argument("--prefilter", type=int, default=0,
@@ -305,7 +314,8 @@ def main(argv=None):
             + f"), launch flags PDL|readonly, "
             f"{args.trials} interleaved trials x {args.replays} graph replays, median"
             + (f", top {args.prefilter} of a first pass (2 trials x 3 replays) timed fully"
-               if args.prefilter else ""))
+               if args.prefilter else "")
+            + (f"; {args.note}" if args.note else ""))
     write_table(entries, args.out, note)
     if args.json:
         with open(args.json, "w") as f:

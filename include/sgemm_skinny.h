@@ -121,7 +121,7 @@ enum {
                                      x rows m and m+1 at the same k, and the diagonal of D is the
                                      per-segment dot product (2 MMAs per 16 bytes of W and pair
                                      of x rows, instead of 8 FMAs per x row) */
-    SGEMM_VARIANT_TC05 = 10       /* the Blackwell tensor-core data path: a producer thread streams
+    SGEMM_VARIANT_TC05 = 10,      /* the Blackwell tensor-core data path: a producer thread streams
                                      boxes of 128 rows x 64 elements of W (and the matching box
                                      of x) with TMA (cp.async.bulk.tensor) into a ring of shared-
                                      memory stages; one thread issues tcgen05.mma (128 rows of W x
@@ -137,6 +137,14 @@ enum {
                                      split_k)) ranges are used) and add their partial sums in
                                      rank order through distributed shared memory: one launch,
                                      no scratch memory */
+    SGEMM_VARIANT_LDG_CLUSTER = 11 /* the kernels of variant 1 with a one-launch split: the split_k
+                                     (2..8) CTAs of a row range form a thread-block cluster; rank
+                                     0 takes the others' FP32 partial sums into its shared memory
+                                     (st.async counted on an mbarrier, a bounded wait) and adds
+                                     them in split order from 0, as the second pass adds, so the
+                                     bits equal variant 1 with the same split.  No scratch memory,
+                                     no second kernel.  Its grid gives each warp one row group at
+                                     most (ctas_per_sm is not used); split_k = 1 is variant 1 */
 };
 
 /* Launch flags (bit set) for the _ex calls.
@@ -153,11 +161,12 @@ enum {
  *   kernel finishes. */
 #define SGEMM_FLAG_PDL 1u
 #define SGEMM_FLAG_WEIGHTS_READONLY 2u
-/* TEST ONLY: the kernel that waits on mbarriers for its copies
- * (SGEMM_VARIANT_TC05) issues no copies, so its bounded waits run out (about
- * 0.2 s each); it then writes NaN outputs, sets the device error word and
- * returns.  Exercises failure detection without a fault.  Other variants
- * ignore the flag. */
+/* TEST ONLY: the kernels that wait on mbarriers make those waits run out
+ * (about 0.2 s each) without any fault: the tcgen05 kernel
+ * (SGEMM_VARIANT_TC05) issues no copies, and in a cluster-split streaming plan
+ * (SGEMM_VARIANT_LDG_CLUSTER, split_k > 1) ranks 1.. send rank 0 no partial
+ * sums.  The kernel then writes NaN outputs, sets the device error word and
+ * returns.  Exercises failure detection.  Other variants ignore the flag. */
 #define SGEMM_FLAG_TEST_STALL 4u
 
 /* y = x . W^T for contiguous x [M,K] and y [M,N].  Plan: sgemm_plan_select(N, K, M). */

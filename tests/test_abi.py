@@ -303,3 +303,22 @@ def test_sweep_candidates_are_valid_plans(lib, N, K, M):
     tc = [p for p in cands if p.variant == sk.SGEMM_VARIANT_TC05]
     assert {p.k_unroll for p in tc} == {1, 2, 3, 4}
     assert {p.stages for p in tc} >= {2, 3, 4}
+
+
+def test_ldg_cluster_plan_checks(lib):
+    """The cluster-split streaming plans (variant 11) run the mixed-precision
+    streaming kernels with at most 8 CTAs per cluster."""
+    base = next(p for p in (sk.sgemm_plan_get(i) for i in range(sk.sgemm_plan_count()))
+                if p.variant == sk.SGEMM_VARIANT_LDG_MIXFMA)
+    cl = base.copy(variant=sk.SGEMM_VARIANT_LDG_CLUSTER)
+    for split in (1, 2, 3, 4, 8):
+        assert sk.sgemm_plan_check(cl.copy(split_k=split), 4, 2048, 4096) == sk.SGEMM_OK, split
+    assert sk.sgemm_plan_check(cl.copy(split_k=9), 4, 2048, 4096) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE
+    # a kernel that only other variants have is refused
+    mma = next(p for p in (sk.sgemm_plan_get(i) for i in range(sk.sgemm_plan_count()))
+               if p.variant == sk.SGEMM_VARIANT_MMA)
+    assert sk.sgemm_plan_check(mma.copy(variant=sk.SGEMM_VARIANT_LDG_CLUSTER, split_k=2), 4,
+                               2048, 4096) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE
+    # the no-allocation call runs such a plan as variant 1 through its array
+    st, p = sk.sgemm_splitk_noalloc_plan(2048, 4096, 2, 4, cl.copy(split_k=2))
+    assert st == sk.SGEMM_OK and p.as_dict() == base.copy(split_k=4).as_dict()

@@ -60,3 +60,32 @@ def test_stalled_kernel_reports_and_context_survives(split):
                   synth.bits(x), synth.bits(W))
     assert rep["ok"], rep
     assert sk.sgemm_device_errors() == 0
+
+
+def test_stalled_cluster_split_streaming_plan_reports_and_context_survives():
+    """The cluster-split streaming plan's one wait (rank 0 for the other ranks'
+    partial sums) runs out when they send none (the test-only flag): NaN
+    outputs, the error bit, and a correct call afterwards."""
+    M, N, K = 3, 2048, 4096
+    x = synth.normal_bf16((M, K), 1.0, seed=11)
+    W = synth.normal_bf16((N, K), 0.02, seed=12)
+    xd, Wd = x.cuda(), W.cuda()
+    base = next(p for p in (sk.sgemm_plan_get(i) for i in range(sk.sgemm_plan_count()))
+                if p.variant == sk.SGEMM_VARIANT_LDG_MIXFMA)
+    plan = base.copy(variant=sk.SGEMM_VARIANT_LDG_CLUSTER, split_k=4)
+    sk.sgemm_device_errors()
+    assert sk.sgemm_device_errors() == 0
+    y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    t0 = time.time()
+    sk.sgemm_bf16_skinny_ex(xd, Wd, y, plan=plan, flags=sk.SGEMM_FLAG_TEST_STALL)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 30, "bounded waits must end"
+    assert torch.isnan(y.float()).all(), "outputs of a stalled reduction must be NaN"
+    assert sk.sgemm_device_errors() & 1
+    assert sk.sgemm_device_errors() == 0
+    y2 = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=plan)
+    torch.cuda.synchronize()
+    rep = compare(synth.bits(y2), oracle.skinny_gemm(synth.bits(x), synth.bits(W)),
+                  synth.bits(x), synth.bits(W))
+    assert rep["ok"], rep
+    assert sk.sgemm_device_errors() == 0
