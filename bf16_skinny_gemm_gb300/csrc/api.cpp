@@ -58,8 +58,6 @@ const KernelInfo *table_for_m(int M) {
 const KernelInfo *find_kernel(int variant, int M, int R, int LPR, int U, int stages) {
     const KernelInfo *t = table_for_m(M);
     if (!t) return nullptr;
-    // the cluster-split plans run the kernels of the mixed-precision streaming plans
-    if (variant == SGEMM_VARIANT_LDG_CLUSTER) variant = SGEMM_VARIANT_LDG_MIXFMA;
     if (variant == SGEMM_VARIANT_TC05) {
         // one kernel per M; the rest are launch parameters
         for (int i = 0; i < sk::kKernelCountPerM; ++i)
@@ -411,7 +409,6 @@ sgemm_status_t run(const sgemm_pair_t *items, int batch, int M, int N, int K,
     prm.split = split;
     prm.row_groups = sk::work_units(plan, N);
     prm.flags = static_cast<int>(flags);
-    prm.cluster = clv ? 1 : 0;
     prm.cl_rows = clv ? sk::cluster_rows(plan) : 0;
 
     int grid_x = 0;

@@ -46,9 +46,8 @@ struct Params {
     int out_f32;     // 1: y holds FP32 outputs (no BF16 rounding)
     int xn_len;      // fused chain epilogue: xn[m][k] for 0 <= k < xn_len ...
     float xn_scale;  // ... = RNE_bf16(float(y[m][k mod N]) * xn_scale)
-    int cluster;     // streaming kernel: the split CTAs of a row range form a thread-block
-                     // cluster and rank 0 adds the partial sums (no ws, no second pass)
-    int cl_rows;     // ... rows per CTA that rank 0's buffer holds per split
+    int cl_rows;     // cluster-split streaming plans: rows per CTA that rank 0's buffer
+                     // holds per split
 };
 
 // Kernel parameters of the TMA + tcgen05 kernel (skinny_tc05.cuh): the common

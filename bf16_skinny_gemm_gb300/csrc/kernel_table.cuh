@@ -64,6 +64,20 @@
      M, R, LPR, U, (DB) ? 2 : 1,                                                          \
      reinterpret_cast<const void *>(&skinny_ldg_kernel<M, R, LPR, U, FMODE, DB>)},
 
+// Cluster-split instantiations of mixed-precision configurations (M, R, LPR,
+// U, double-buffered): the split CTAs of a row range form a thread-block
+// cluster and rank 0 adds the partial sums (SGEMM_VARIANT_LDG_CLUSTER).
+#define SK_LDGCL_CONFIGS(X, M) \
+    X(M, 1, 32, 8, false)      \
+    X(M, 1, 32, 4, true)       \
+    X(M, 2, 32, 4, false)      \
+    X(M, 2, 32, 2, true)       \
+    X(M, 4, 32, 2, false)
+
+#define SK_LDGCL_ENTRY(M, R, LPR, U, DB)                             \
+    {SGEMM_VARIANT_LDG_CLUSTER, M, R, LPR, U, (DB) ? 2 : 1,          \
+     reinterpret_cast<const void *>(&skinny_ldg_kernel<M, R, LPR, U, 1, DB, false, true>)},
+
 // Tensor-core configurations: (M, k-blocks per batch U, double-buffered).
 // R = 16 rows per tile, 4 lanes share a row segment.
 #define SK_MMA_CONFIGS(X, M) \
@@ -86,4 +100,5 @@
 
 #define SK_DEFINE_TABLE(M, NAME)                                                          \
     const KernelInfo NAME[] = {SK_LDG_CONFIGS(SK_LDG_ENTRY, M) SK_MMA_CONFIGS(SK_MMA_ENTRY, M) \
-                                   SK_LDGX_CONFIGS(SK_LDGX_ENTRY, M) SK_TC05_ENTRY(M)};
+                                   SK_LDGX_CONFIGS(SK_LDGX_ENTRY, M)                       \
+                                       SK_LDGCL_CONFIGS(SK_LDGCL_ENTRY, M) SK_TC05_ENTRY(M)};

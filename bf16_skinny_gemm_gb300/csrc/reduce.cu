@@ -6,8 +6,9 @@ namespace sk {
 #define SK_COUNT_ONE(M, R, LPR, U, FMODE, DB) +1
 #define SK_COUNT_MMA(M, U, DB) +1
 #define SK_COUNT_LDGX(M, R, LPR, U, FMODE) +1
+#define SK_COUNT_LDGCL(M, R, LPR, U, DB) +1
 const int kKernelCountPerM = 0 SK_LDG_CONFIGS(SK_COUNT_ONE, 1) SK_MMA_CONFIGS(SK_COUNT_MMA, 1)
-    SK_LDGX_CONFIGS(SK_COUNT_LDGX, 1) + 1 /* TMA + tcgen05 */;
+    SK_LDGX_CONFIGS(SK_COUNT_LDGX, 1) SK_LDGCL_CONFIGS(SK_COUNT_LDGCL, 1) + 1 /* TMA + tcgen05 */;
 
 const void *const kReduceKernels[kMaxM + 1] = {
     nullptr,

@@ -414,7 +414,7 @@ struct XChunk<M, 3> {
     }
 };
 
-template <int M, int R, int LPR, int U, int FMODE, bool DB, bool XG = false>
+template <int M, int R, int LPR, int U, int FMODE, bool DB, bool XG = false, bool CL = false>
 __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_constant__ Params p) {
     static_assert(LPR == 32 || LPR == 16 || LPR == 8, "lanes per row");
     static_assert(FMODE != 3 || LPR == 32, "the tensor-core mode spreads a row over the warp");
@@ -443,12 +443,13 @@ __global__ void __launch_bounds__(kMaxThreads) skinny_ldg_kernel(const __grid_co
     const int g0 = g_begin + warp;
     const int ntask = g0 < g_end ? (g_end - g0 + warps - 1) / warps : 0;
 
-    // Split across a thread-block cluster (p.cluster): the p.split CTAs of this row range
-    // form a cluster, rank r having K split r.  Rank 0 keeps its own partial sums and takes
+    // Split across a thread-block cluster (CL, compiled only for the cluster-split plans,
+    // so the other plans' code is unchanged): the p.split CTAs of this row range form a
+    // cluster, rank r having K split r.  Rank 0 keeps its own partial sums and takes
     // the other ranks' through st.async into red [split][cl_rows][M], every byte counted on
     // its mbarrier cl_bar; it adds them in split order once they have landed.
     __shared__ __align__(8) uint64_t cl_bar;
-    const bool cl = p.cluster != 0 && p.split > 1;
+    const bool cl = CL && p.split > 1;
     const int crank = cl ? static_cast<int>(cluster_rank()) : 0;
     const int row0 = g_begin * G * R;
     const int rows_valid = max(0, min(p.N, g_end * G * R) - row0);

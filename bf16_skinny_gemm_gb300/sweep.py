@@ -66,11 +66,8 @@ def candidates(M, N, K, splits, ctas=(0,)):
     out = []
     for i in range(sk.sgemm_plan_count()):
         base = sk.sgemm_plan_get(i)
-        if base.variant == sk.SGEMM_VARIANT_LDG_MIXFMA:
-            # also as the cluster-split plan (one launch, no second pass)
-            variants = [base.copy(split_k=s, ctas_per_sm=c) for s in splits for c in ctas]
-            variants += [base.copy(variant=sk.SGEMM_VARIANT_LDG_CLUSTER, split_k=s)
-                         for s in LDG_CLUSTER_SPLITS]
+        if base.variant == sk.SGEMM_VARIANT_LDG_CLUSTER:
+            variants = [base.copy(split_k=s) for s in LDG_CLUSTER_SPLITS]
         elif base.variant == sk.SGEMM_VARIANT_TC05:
             if base.k_unroll != 1:
                 continue  # the enumeration lists this kernel twice; its geometry is swept here

@@ -306,15 +306,15 @@ def test_sweep_candidates_are_valid_plans(lib, N, K, M):
 
 
 def test_ldg_cluster_plan_checks(lib):
-    """The cluster-split streaming plans (variant 11) run the mixed-precision
-    streaming kernels with at most 8 CTAs per cluster."""
-    base = next(p for p in (sk.sgemm_plan_get(i) for i in range(sk.sgemm_plan_count()))
-                if p.variant == sk.SGEMM_VARIANT_LDG_MIXFMA)
-    cl = base.copy(variant=sk.SGEMM_VARIANT_LDG_CLUSTER)
+    """The cluster-split streaming plans (variant 11): the cluster instantiations
+    of mixed-precision streaming configurations, at most 8 CTAs per cluster."""
+    cl = next(p for p in (sk.sgemm_plan_get(i) for i in range(sk.sgemm_plan_count()))
+              if p.variant == sk.SGEMM_VARIANT_LDG_CLUSTER)
+    base = cl.copy(variant=sk.SGEMM_VARIANT_LDG_MIXFMA)
     for split in (1, 2, 3, 4, 8):
         assert sk.sgemm_plan_check(cl.copy(split_k=split), 4, 2048, 4096) == sk.SGEMM_OK, split
     assert sk.sgemm_plan_check(cl.copy(split_k=9), 4, 2048, 4096) == sk.SGEMM_ERR_UNSUPPORTED_SHAPE
-    # a kernel that only other variants have is refused
+    # a configuration compiled only for other variants is refused
     mma = next(p for p in (sk.sgemm_plan_get(i) for i in range(sk.sgemm_plan_count()))
                if p.variant == sk.SGEMM_VARIANT_MMA)
     assert sk.sgemm_plan_check(mma.copy(variant=sk.SGEMM_VARIANT_LDG_CLUSTER, split_k=2), 4,

@@ -71,8 +71,8 @@ def test_stalled_cluster_split_streaming_plan_reports_and_context_survives():
     W = synth.normal_bf16((N, K), 0.02, seed=12)
     xd, Wd = x.cuda(), W.cuda()
     base = next(p for p in (sk.sgemm_plan_get(i) for i in range(sk.sgemm_plan_count()))
-                if p.variant == sk.SGEMM_VARIANT_LDG_MIXFMA)
-    plan = base.copy(variant=sk.SGEMM_VARIANT_LDG_CLUSTER, split_k=4)
+                if p.variant == sk.SGEMM_VARIANT_LDG_CLUSTER)
+    plan = base.copy(split_k=4)
     sk.sgemm_device_errors()
     assert sk.sgemm_device_errors() == 0
     y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")

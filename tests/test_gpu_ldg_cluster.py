@@ -21,9 +21,15 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _mixfma_plans():
+def _cl_plans():
+    """The compiled cluster-split plans (one per configuration and CTA size)."""
     return [p for p in (sk.sgemm_plan_get(i) for i in range(sk.sgemm_plan_count()))
-            if p.variant == sk.SGEMM_VARIANT_LDG_MIXFMA]
+            if p.variant == sk.SGEMM_VARIANT_LDG_CLUSTER]
+
+
+def _two_kernel(p):
+    """The same configuration as a variant-1 plan: scratch split plus second pass."""
+    return p.copy(variant=sk.SGEMM_VARIANT_LDG_MIXFMA)
 
 
 def _inputs(M, N, K, seed):
@@ -53,9 +59,11 @@ def test_every_kernel_matches_two_kernel_split(M, split):
     xd, Wd = x.to(DEV), W.to(DEV)
     xb, Wb = synth.bits(x), synth.bits(W)
     ref = oracle.skinny_gemm(xb, Wb)
-    for p in _mixfma_plans():
-        two = p.copy(split_k=split)
-        one = two.copy(variant=sk.SGEMM_VARIANT_LDG_CLUSTER)
+    plans = _cl_plans()
+    assert plans
+    for p in plans:
+        one = p.copy(split_k=split)
+        two = _two_kernel(one)
         assert sk.sgemm_plan_check(one, M, N, K) == sk.SGEMM_OK, one
         y1 = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=one)
         y2 = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=two)
@@ -71,14 +79,14 @@ def test_every_kernel_matches_two_kernel_split(M, split):
 def test_shapes(M, N, K):
     x, W = _inputs(M, N, K, seed=600 + N)
     xd, Wd = x.to(DEV), W.to(DEV)
-    for p in _mixfma_plans()[:4]:
+    for p in _cl_plans()[:4]:
         for split in (2, 4):
-            one = p.copy(variant=sk.SGEMM_VARIANT_LDG_CLUSTER, split_k=split)
+            one = p.copy(split_k=split)
             if sk.sgemm_plan_check(one, M, N, K) != sk.SGEMM_OK:
                 assert K < 8 * 2 * split, (one, N, K)  # too few 8-element chunks to split
                 continue
             y = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=one)
-            y2 = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=one.copy(variant=sk.SGEMM_VARIANT_LDG_MIXFMA))
+            y2 = sk.sgemm_bf16_skinny_ex(xd, Wd, plan=_two_kernel(one))
             torch.cuda.synchronize()
             assert _eq(y, y2), one
             if N * K <= 4096 * 1024:
@@ -90,7 +98,7 @@ def test_shapes(M, N, K):
 def test_strided_batched_and_epilogues():
     from tolerance import compare_f32
     M, N, K, batch = 3, 1111, 2048, 3
-    one = _mixfma_plans()[0].copy(variant=sk.SGEMM_VARIANT_LDG_CLUSTER, split_k=4)
+    one = _cl_plans()[0].copy(split_k=4)
     act = synth.normal_bf16((M, batch * K), 1.0, seed=700).to(DEV)
     xs = act.unflatten(1, (batch, K)).transpose(0, 1)
     Ws = [synth.normal_bf16((N, K), synth.W_STD, seed=701 + i).to(DEV) for i in range(batch)]
@@ -124,8 +132,8 @@ def test_pdl_chain_and_graph(flags):
     shapes = [(4096, 4096), (2048, 4096), (4096, 2048), (8192, 4096)]  # N_i >= K_{i+1}
     Ws = [synth.normal_bf16(s, synth.W_STD, seed=800 + i).to(DEV) for i, s in enumerate(shapes)]
     x0 = synth.normal_bf16((M, 4096), 1.0, seed=799).to(DEV)
-    base = _mixfma_plans()[0]
-    plans = [base.copy(variant=sk.SGEMM_VARIANT_LDG_CLUSTER, split_k=s) for s in (4, 2, 3, 8)]
+    base = _cl_plans()[0]
+    plans = [base.copy(split_k=s) for s in (4, 2, 3, 8)]
 
     def chain(fl):
         outs, x = [], x0
