@@ -319,7 +319,9 @@ sgemm_status_t sgemm_bf16_skinny_splitk_noalloc(const sgemm_bf16_t *x, long long
  * that way are replaced: a TMA + tcgen05 plan (SGEMM_VARIANT_TC05, whose split
  * reduces inside a cluster) by the CUDA-core streaming plan (variant
  * SGEMM_VARIANT_LDG_MIXFMA, 256 threads, 1 row per warp, 32 lanes per row,
- * k_unroll 8, 1 stage).  Pure host function.  Writes *out
+ * k_unroll 8, 1 stage), and a cluster-split streaming plan
+ * (SGEMM_VARIANT_LDG_CLUSTER) by the same configuration as variant
+ * SGEMM_VARIANT_LDG_MIXFMA.  Pure host function.  Writes *out
  * and returns sgemm_plan_check of it for (M, N, K); SGEMM_ERR_INVALID_ARG for
  * a NULL out or split_k < 2. */
 sgemm_status_t sgemm_splitk_noalloc_plan(int N, int K, int M, int split_k,
